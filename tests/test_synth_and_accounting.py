@@ -1,0 +1,80 @@
+"""Generator determinism / recipe checks and the byte/FLOP accounting pinned to
+the figures printed on the source pages (tests/golden/page_figures.json)."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from moe_expert_ffn_02_gb300 import roofline
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "page_figures.json")
+
+
+def test_generator_is_counter_based_and_deterministic():
+    a = synth.bf16_normal(0, synth.STREAM_X, (4, 1024))
+    b = synth.bf16_normal(0, synth.STREAM_X, (4, 1024))
+    assert np.array_equal(a, b)
+    c = synth.bf16_normal(0, synth.STREAM_X, (8, 1024))
+    assert np.array_equal(c[:4], a)                           # prefix-stable
+    assert not np.array_equal(synth.bf16_normal(1, synth.STREAM_X, (4, 1024)), a)
+    assert not np.array_equal(synth.bf16_normal(0, synth.STREAM_ROUTER_W, (4, 1024)), a)
+    q1, s1 = synth.fp8_blocks(0, synth.STREAM_GATE, 3, 256, 384)
+    q2, s2 = synth.fp8_blocks(0, synth.STREAM_GATE, 2, 256, 384)
+    assert np.array_equal(q1[:2], q2) and np.array_equal(s1[:2], s2)
+
+
+def test_generator_distributions():
+    x = synth.bf16_to_f32(synth.bf16_normal(0, synth.STREAM_X, (256, 1024))).astype(np.float64)
+    assert abs(x.mean()) < 0.01 and abs(x.std() - 1.0) < 0.01 and np.abs(x).max() <= 6.0
+    q, s = synth.fp8_blocks(0, synth.STREAM_GATE, 2, 256, 512, std=0.02)
+    w = oracle.e4m3_decode(q) * np.repeat(np.repeat(s.astype(np.float64), 128, 1), 128, 2)
+    assert abs(w.std() - 0.02) < 0.001
+    # every block's multiplier is its amax / 448, so its largest code is +-448
+    blk = q.reshape(2, 2, 128, 4, 128).transpose(0, 1, 3, 2, 4).reshape(2, 2, 4, -1)
+    assert np.all((blk & 0x7F).max(-1) == 0x7E)
+
+
+def test_zipf_bias_recipe_gives_skewed_load():
+    """Skewed 32K prefill workload: popularity must put hot experts above
+    10x the mean row count and leave some experts with no rows."""
+    wl = synth.WORKLOADS["skew_32k"]
+    b = synth.router_bias(wl, seed=0)
+    assert b.shape == (wl.n_experts,) and np.isclose(b.max(), 0.0)
+    # logits ~ N(0,1) (router std 1/sqrt(H) on N(0,1) activations) plus the bias
+    L = (np.random.default_rng(0).normal(0, 1, (wl.T, wl.n_experts)) + b).astype(np.float32)
+    r = oracle.route_from_logits(L, wl.top_k)
+    counts = np.diff(r["offsets"])
+    mean = wl.T * wl.top_k / wl.n_experts
+    assert counts.max() > 10 * mean
+    assert np.count_nonzero(counts == 0) > 0
+
+
+def test_page_figures_pin_accounting():
+    fig = {e["name"]: e for e in json.load(open(GOLDEN))["entries"]}
+
+    def close(name, got):
+        e = fig[name]
+        assert abs(got - e["value"]) <= e["rel_tol"] * e["value"] + 1e-9, (name, got, e["value"])
+
+    close("params_per_expert", roofline.expert_params(7168, 2048))
+    close("active_routed_params_per_token", 58 * 8 * roofline.expert_params(7168, 2048))
+    close("routed_params_model", 58 * 256 * roofline.expert_params(7168, 2048))
+    close("layer_expert_bytes_deepseek_v3", roofline.layer_expert_bytes(7168, 2048, 256))
+    close("layer_expert_bytes_kimi_k2", roofline.layer_expert_bytes(7168, 2048, 384))
+    close("weight_tensor_count_deepseek_v3", 58 * 256 * 3)
+    close("tokens_per_routed_expert_b64", roofline.tokens_per_routed_expert(64, 8, 256))
+    close("active_routed_bytes_per_token_4p5bit", 58 * 8 * roofline.expert_params(7168, 2048) * 4.5 / 8)
+
+
+def test_flop_and_touched_byte_accounting():
+    # 2 * 3 * H * I per (token, expert) pair, k routed + 1 shared per token
+    assert roofline.layer_flops(8192, 7168, 2048, 8, 1) == 88_080_384 * 8192 * 9
+    assert abs(roofline.expected_distinct_experts(16, 8, 256) - 256 * (1 - (31 / 32) ** 16)) < 1e-9
+    ids = np.array([[0, 3], [3, 5]])
+    assert roofline.touched_experts(ids, 8) == 3
+    eb = roofline.expert_bytes(7168, 2048)
+    assert eb == 44_040_192 + 3 * 56 * 16 * 4
+    assert roofline.decode_weight_bytes(ids, 7168, 2048, 8, 1) == 4 * eb
