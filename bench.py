@@ -1,0 +1,386 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 MoE FFN layer (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one whole layer (router logits, top-k, grouping, activation
+quantisation, gate/up GEMM + SiLU*up, down GEMM, combine) over the
+workload's T tokens, on seeded synthetic inputs of the workload's shapes.
+Default workload: the DeepSeek-V3-shaped decode layer with T = 16 tokens
+(metric: microseconds per layer, lower is better).  Prefill workloads report
+tokens per second.
+
+Device timing: CUDA events around every step on the launching stream, after
+W warm-up steps; L2 is flushed (512 MiB write) between steps, outside the
+timed events.  The dominant kernel's duration comes from the library's
+per-stage events inside each timed step.  e2e: the same layer through
+moe_forward_host from pinned host buffers (copies included).  cpu_baseline:
+the CPU oracle on the host cores, on a bounded sample of the workload.
+
+--impl reference times the CPU oracle itself (there is no other reference
+implementation of this layer) on the same workload and prints the same line
+with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+from moe_expert_ffn_02_gb300 import roofline  # noqa: E402
+
+MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FP8_OVER_BF16 = 2.0          # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default="ds_decode_t16", choices=sorted(synth.WORKLOADS))
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    a = p.parse_args()
+    a.warmup = max(a.warmup, 3)
+    return a
+
+
+def peaks():
+    try:
+        d = json.load(open(MEASURED_PEAKS))
+        return {"hbm": float(d["hbm_gbs"]), "bf16": float(d["bf16_tflops"]),
+                "bf16_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "src": "measured"}
+    except Exception:
+        return {"hbm": FALLBACK_HBM_GBS, "bf16": FALLBACK_BF16_TFLOPS, "bf16_sustained": 1700.0, "src": "fallback"}
+
+
+def is_decode(wl) -> bool:
+    return wl.T <= 64
+
+
+def metric_of(wl):
+    if is_decode(wl):
+        return "moe_layer_decode_us_per_layer", "us/layer", False
+    return "moe_layer_prefill_tokens_per_s", "tokens/s", True
+
+
+def value_of(wl, seconds_per_step: float, n_ranks: int = 1):
+    if is_decode(wl):
+        return seconds_per_step * 1e6
+    return wl.T * n_ranks / seconds_per_step
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.rows, self.proc = index, [], None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if len(r) > 4 + i and r[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "moe_expert_ffn_02_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str, workload: str):
+    """dram bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    try:
+        d = json.load(open(TRAFFIC_FILE))
+    except Exception:
+        return None
+    e = d.get(workload, {}).get(kernel)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample_plan(wl, target_s: float = 15.0):
+    """Tokens per oracle call and number of calls for ~target_s of CPU work."""
+    import oracle
+    per_token_macs = 3 * wl.hidden * wl.inter * (wl.top_k + wl.n_shared) + wl.hidden * wl.n_experts
+    rate = 0.6e9 * oracle.threads()          # rough fp64 MAC/s of the oracle per core
+    tokens = max(1, min(wl.T, int(target_s * rate / per_token_macs)))
+    return tokens
+
+
+def time_oracle(wl, inp, rows, repeats=1):
+    """Wall time of the oracle layer (logits + routing + experts + combine) on `rows`."""
+    import oracle
+    sub = dict(inp, x=inp["x"][rows])
+    best = None
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        L = oracle.logits(sub["x"], inp["router_w"], inp["router_b"])
+        r = oracle.route_from_logits(L, wl.top_k)
+        oracle.forward(sub, wl.top_k, r["ids"], r["w"])
+        dt = time.perf_counter() - t0
+        best = dt if best is None else min(best, dt)
+    return best
+
+
+def cpu_value(wl, seconds: float, n_tokens: int):
+    """Oracle throughput in the workload's unit (decode: us for a T-token layer)."""
+    if is_decode(wl):
+        return seconds / n_tokens * wl.T * 1e6
+    return n_tokens / seconds
+
+
+# ---------------------------------------------------------------------------- reference arm
+
+def run_reference(a, wl):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    metric, unit, hib = metric_of(wl)
+    inp = synth.make_inputs(wl, seed=a.seed)
+    n_tok = min(wl.T, max(1, oracle_sample_plan(wl, target_s=60.0 / max(1, a.steps + a.warmup))))
+    rows = np.arange(n_tok)
+    for _ in range(a.warmup):
+        time_oracle(wl, inp, rows[: max(1, n_tok // 4)])
+    times = [time_oracle(wl, inp, rows) for _ in range(a.steps)]
+    sec = sum(times) / len(times)
+    v = cpu_value(wl, sec, n_tok)
+    line = {
+        "impl": "reference", "metric": metric, "value": v, "unit": unit, "n_gpus": a.gpus, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": sec * 1e3, "higher_is_better": hib, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "T": wl.T, "hidden": wl.hidden, "inter": wl.inter,
+                   "n_experts": wl.n_experts, "top_k": wl.top_k, "n_shared": wl.n_shared},
+        "cpu_baseline": {"value": v, "unit": unit, "cores": oracle.threads(), "kind": "oracle",
+                         "sample": f"first {n_tok} of {wl.T} tokens per step, scaled to the workload"},
+        "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------- our arm
+
+def run_ours(a, wl):
+    import torch
+    import torch.distributed as dist
+
+    import moe_expert_ffn_02_gb300 as moe
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    moe.load()
+    metric, unit, hib = metric_of(wl)
+    inp = synth.make_inputs(wl, seed=a.seed)
+    dev = {k: (torch.from_numpy(np.ascontiguousarray(v)).cuda() if v is not None else None)
+           for k, v in inp.items() if k != "x"}
+    layer = moe.Layer(wl.hidden, wl.inter, wl.n_experts, wl.top_k, dev, n_shared=wl.n_shared)
+    del dev
+    torch.cuda.empty_cache()
+    T, H = wl.T, wl.hidden
+    mode = moe.MODE_DECODE if is_decode(wl) else moe.MODE_PREFILL
+    stream = torch.cuda.current_stream()
+    x = torch.from_numpy(inp["x"].view(np.int16)).cuda()
+    y = torch.empty_like(x)
+    ws, nbytes = layer.workspace(T, mode)
+    fwd = moe.moe_forward_decode if mode == moe.MODE_DECODE else moe.moe_forward_prefill
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def step():
+        fwd(layer.handle, x.data_ptr(), T, y.data_ptr(), None, ws, nbytes, stream.cuda_stream)
+
+    # routing of this workload (for the algorithmic-byte count)
+    ids = torch.empty((T, wl.top_k), dtype=torch.int32, device="cuda")
+    moe.moe_forward_prefill(layer.handle, x.data_ptr(), T, y.data_ptr(), {"topk_ids": ids.data_ptr()}, ws, nbytes,
+                            stream.cuda_stream)
+    ids_np = ids.cpu().numpy()
+    st, flags = moe.moe_get_device_status(layer.handle, stream.cuda_stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} flags {flags:#x}")
+
+    for _ in range(a.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    moe.moe_profile_enable(layer.handle, True)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
+    stage_ms = []
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        for i in range(a.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+            stage_ms.append(moe.moe_profile_read(layer.handle))
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    moe.moe_profile_enable(layer.handle, False)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_s = sum(step_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([total_s], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_s = float(t.item())
+        dist.barrier()
+    sec_per_step = total_s / a.steps
+    value = value_of(wl, sec_per_step, world)
+    n_launches = 9 * a.steps          # logits, top-k, 3 grouping, quantise, gate/up, down, combine
+
+    # ---------------------------------------------- roofline of the dominant kernel
+    pk = peaks()
+    mean_stage = {k: statistics.mean(s[k] for s in stage_ms) for k in stage_ms[0]}
+    dom = "gate_up" if mean_stage["gate_up"] >= mean_stage["down"] else "down"
+    dom_s = mean_stage[dom] / 1e3
+    n_touched = roofline.touched_experts(ids_np, wl.n_experts) + wl.n_shared
+    rows = T * wl.top_k + T * wl.n_shared
+    if is_decode(wl):
+        if dom == "gate_up":
+            alg = roofline.decode_gate_up_bytes(ids_np, H, wl.inter, wl.n_experts, wl.n_shared) + rows * (H + wl.inter)
+        else:
+            alg = n_touched * (H * wl.inter + (H // 128) * (wl.inter // 128) * 4) + rows * (wl.inter + 4 * H)
+        achieved = alg / dom_s / 1e9
+        roof = {"bound": "hbm", "kernel": f"expert_gemm_kernel<{'true' if dom == 'gate_up' else 'false'}>",
+                "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s", "frac": achieved / pk["hbm"],
+                "algorithmic_bytes_per_launch": alg, "peak_source": pk["src"],
+                "traffic": traffic_for(dom, wl.name)}
+    else:
+        flops_all = roofline.layer_flops(T, H, wl.inter, wl.top_k, wl.n_shared)
+        alg = flops_all * (2 / 3 if dom == "gate_up" else 1 / 3)
+        achieved = alg / dom_s / 1e12
+        peak = pk["bf16"] * FP8_OVER_BF16
+        roof = {"bound": "tensor", "kernel": f"expert_gemm_kernel<{'true' if dom == 'gate_up' else 'false'}>",
+                "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "algorithmic_flops_per_launch": alg,
+                "peak_source": f"{pk['src']} bf16 burst x {FP8_OVER_BF16} (nominal fp8/bf16 dense ratio)",
+                "traffic": traffic_for(dom, wl.name)}
+
+    # ---------------------------------------------- end to end through the host entry
+    e2e = None
+    if not a.no_e2e:
+        xh = torch.from_numpy(inp["x"].view(np.int16)).pin_memory()
+        yh = torch.empty_like(xh).pin_memory()
+        ws_h, nb_h = layer.workspace(T, mode)
+        for _ in range(2):
+            moe.moe_forward_host(layer.handle, mode, xh.data_ptr(), T, yh.data_ptr(), ws_h, nb_h, stream.cuda_stream)
+        e_ms = []
+        for _ in range(a.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            moe.moe_forward_host(layer.handle, mode, xh.data_ptr(), T, yh.data_ptr(), ws_h, nb_h, stream.cuda_stream)
+            e1.record(stream)
+            e1.synchronize()
+            e_ms.append(e0.elapsed_time(e1))
+        e2e = {"value": value_of(wl, statistics.mean(e_ms) / 1e3, world), "unit": unit,
+               "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2}
+
+    # ---------------------------------------------- CPU oracle baseline (rank 0, N = 1)
+    cpu = None
+    if not a.no_cpu_baseline and rank == 0 and world == 1:
+        import oracle
+        oracle.build()
+        n_tok = oracle_sample_plan(wl, target_s=12.0)
+        rows_s = np.arange(n_tok)
+        sec = time_oracle(wl, inp, rows_s)
+        cpu = {"value": cpu_value(wl, sec, n_tok), "unit": unit, "cores": oracle.threads(), "kind": "oracle",
+               "sample": f"first {n_tok} of {T} tokens (logits, routing, experts, combine), scaled to the workload"}
+
+    layer.close()
+    if rank == 0:
+        line = {
+            "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
+            "ms_per_step": sec_per_step * 1e3, "higher_is_better": hib, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp8_e4m3", "data": "synthetic",
+            "config": {"workload": wl.name, "T": T, "hidden": H, "inter": wl.inter, "n_experts": wl.n_experts,
+                       "top_k": wl.top_k, "n_shared": wl.n_shared, "parallelism": f"replicas{world}",
+                       "l2": "flushed between steps (512 MiB write, outside the timed events)"},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_launches * world,
+            "clocks": clk.summary(), "stage_ms": mean_stage, "touched_experts": n_touched,
+            "wall_s_timed_region": t_wall, "tokens_per_s": T * world / sec_per_step,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    a = parse()
+    wl = synth.WORKLOADS[a.workload]
+    if a.impl == "reference":
+        return run_reference(a, wl)
+    return run_ours(a, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

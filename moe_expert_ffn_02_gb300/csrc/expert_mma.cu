@@ -1,0 +1,474 @@
+// Grouped FP8 expert GEMMs on sm_103a (weight-streaming path).
+//
+// One persistent CTA per SM walks the units (group, n tile of <= 64 rows,
+// m tile of 128 output features).  A producer warp streams, for every
+// 128-wide K block, the 128x128 weight tile image(s) with one bulk copy and
+// the unit's activation rows (128 B each) with per-row bulk copies into a
+// ring of shared-memory stages guarded by mbarriers; eight consumer warps
+// run FP8 E4M3 tensor-core MMAs (m16n8k32, fp32 accumulate) on each stage.
+//
+// Scale promotion follows the post-scaling order of the FP8 GEMV section
+// of the CPU-GPU hybrid inference article (xingyun.xin, Fig. 9-10): the
+// products inside one 128-block are accumulated first (by the tensor core),
+// then the block is scaled once, here by s_w[block] * s_a[row][block], and
+// added to the fp32 accumulator.
+//
+// Gate/up kernel: both projections of the same 128 rows of the expert's
+// inner dimension share the activation fragments; the epilogue forms
+// h = SiLU(g) * u (the activation and elementwise product that sit between
+// gate/up and down in the article's "CPU fine-grained parallelism"
+// section), quantises each token's 128 values of h to E4M3 with
+// s = amax/448, and writes the codes and the scale.  Down kernel: writes the
+// unweighted fp32 expert output rows.
+//
+// K permutation inside a 128-block: lane (g, q) of a warp owns the 32
+// consecutive channels [32q, 32q+32) of the block; MMA m (0..3) takes
+// channels 32q+8m .. 32q+8m+7 of them as its k-slots {4q..4q+3,
+// 16+4q..16+4q+3}.  The same map is applied to the weight rows and to the
+// activation rows, so the dot products are unchanged while every operand
+// fragment comes from two 16-byte shared-memory loads.
+#include "moe_internal.cuh"
+
+namespace moe {
+
+constexpr int BN = 64;                  // rows (tokens) per n tile
+constexpr int CW = 8;                   // consumer warps (16 output rows each)
+constexpr int NTHREADS = (CW + 1) * 32; // + producer warp
+constexpr int XSTRIDE = 144;            // padded activation row in shared memory
+
+template <bool GU>
+struct Cfg {
+    static constexpr int W_BYTES = GU ? 2 * TILE_BYTES : TILE_BYTES;
+    static constexpr int X_BYTES = BN * XSTRIDE;
+    static constexpr int STAGE = W_BYTES + X_BYTES;
+    static constexpr int STAGES = GU ? 4 : 6;
+    static constexpr int EPI = GU ? (BN * 144 + CW * BN * 4) : (BN * 132 * 4);
+    static constexpr int SMEM = STAGES * STAGE + EPI + 2 * STAGES * 8 + 128;
+};
+
+struct ExpertArgs {
+    const uint8_t* w;         // tile images of all groups
+    const float* wscale;      // per (group, m tile, k tile) [x2 for gate/up]
+    const uint8_t* act;       // activation rows [rows_pad][K] (E4M3)
+    const float* actsT;       // activation scales [K/128][ld]
+    int ld;                   // row stride of actsT / shT (rows_pad)
+    int K, M;                 // reduction length, output features
+    const GroupTable* gt;
+    uint8_t* hq;              // gate/up: [rows][M] E4M3 h
+    float* shT;               // gate/up: [M/128][ld]
+    float* out;               // down: [rows][M] fp32
+    uint32_t* status;
+    uint32_t wait_limit;
+};
+
+struct Unit {
+    int expert, mb, row_begin, valid;
+};
+
+__device__ __forceinline__ Unit decode_unit(const GroupTable* gt, int u, int MT) {
+    const int pair = u / MT;
+    Unit r;
+    r.mb = u - pair * MT;
+    int lo = 0, hi = gt->n_groups - 1;           // last group with pair_start <= pair
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (gt->pair_start[mid] <= pair) lo = mid; else hi = mid - 1;
+    }
+    const int nt = pair - gt->pair_start[lo];
+    r.expert = gt->expert[lo];
+    r.row_begin = gt->row0[lo] + nt * BN;
+    r.valid = min(BN, gt->rows[lo] - nt * BN);
+    return r;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+
+template <bool GU>
+__global__ void __launch_bounds__(NTHREADS, 1) expert_gemm_kernel(ExpertArgs a) {
+    using C = Cfg<GU>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* stages = smem;
+    uint8_t* epi = smem + C::STAGES * C::STAGE;
+    uint64_t* full = reinterpret_cast<uint64_t*>(epi + C::EPI);
+    uint64_t* empty = full + C::STAGES;
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int MT = a.M / QB, KT = a.K / QB;
+    const GroupTable* gt = a.gt;
+    const int n_units = gt->n_pairs * MT;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], CW);
+        }
+        fence_mbar_init();
+        abort_flag = 0;
+    }
+    __syncthreads();
+    volatile int* abort = &abort_flag;
+
+    if (warp == CW) {
+        // ------------------------------------------------------------ producer
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t armed = 0, armed_par = 0;       // per stage: armed at least once / parity of last arm
+        bool ok = true;
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            const Unit un = decode_unit(gt, u, MT);
+            const uint8_t* wbase = a.w + ((size_t)(un.expert * MT + un.mb) * KT) * C::W_BYTES;
+            for (int kb = 0; kb < KT; ++kb) {
+                if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, a.wait_limit, a.status, abort)) { ok = false; break; }
+                uint8_t* st = stages + stage * C::STAGE;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&full[stage], C::W_BYTES + un.valid * QB);
+                    bulk_g2s(st, wbase + (size_t)kb * C::W_BYTES, C::W_BYTES, &full[stage]);
+                }
+                __syncwarp();
+                for (int r = lane; r < un.valid; r += 32)
+                    bulk_g2s(st + C::W_BYTES + r * XSTRIDE, a.act + (size_t)(un.row_begin + r) * a.K + kb * QB, QB,
+                             &full[stage]);
+                armed |= 1u << stage;
+                armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+                if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+        // drain: every armed stage's copies must have landed before exit
+        for (int s = 0; s < C::STAGES; ++s)
+            if ((armed >> s) & 1u) mbar_wait_bounded(&full[s], (armed_par >> s) & 1u, a.wait_limit, a.status, nullptr);
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int g = lane >> 2, q = lane & 3;
+    const int r0 = warp * 16 + g;             // tile rows r0 and r0 + 8 (same swizzle phase g)
+    const int c0 = ((2 * q) ^ g) * 16, c1 = ((2 * q + 1) ^ g) * 16;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool dead = false;    // a wait gave up: skip the math, keep the barriers
+
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+        const Unit un = decode_unit(gt, u, MT);
+        const int nt_active = (un.valid + 7) >> 3;
+        const float* wsc = a.wscale + ((size_t)(un.expert * MT + un.mb) * KT) * (GU ? 2 : 1);
+        float accg[BN / 8][4], accu[BN / 8][4];
+#pragma unroll
+        for (int nt = 0; nt < BN / 8; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) { accg[nt][i] = 0.f; accu[nt][i] = 0.f; }
+
+        for (int kb = 0; kb < KT; ++kb) {
+            // activation scales of this lane's columns for block kb
+            float sa[BN / 8][2];
+#pragma unroll
+            for (int nt = 0; nt < BN / 8; ++nt)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int col = nt * 8 + 2 * q + j;
+                    sa[nt][j] = (col < un.valid) ? __ldg(a.actsT + (size_t)kb * a.ld + un.row_begin + col) : 0.f;
+                }
+            const float swg = __ldg(wsc + (size_t)kb * (GU ? 2 : 1));
+            const float swu = GU ? __ldg(wsc + (size_t)kb * 2 + 1) : 0.f;
+
+            if (!dead && !mbar_wait_bounded(&full[stage], phase, a.wait_limit, a.status, abort)) dead = true;
+            if (dead) {
+                if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+                continue;
+            }
+            const uint8_t* st = stages + stage * C::STAGE;
+            const uint8_t* X = st + C::W_BYTES;
+            const uint4 ag0 = lds128(st + r0 * 128 + c0), ag1 = lds128(st + r0 * 128 + c1);
+            const uint4 ag8 = lds128(st + (r0 + 8) * 128 + c0), ag9 = lds128(st + (r0 + 8) * 128 + c1);
+            const uint32_t Ag[8] = {ag0.x, ag0.y, ag0.z, ag0.w, ag1.x, ag1.y, ag1.z, ag1.w};
+            const uint32_t Ah[8] = {ag8.x, ag8.y, ag8.z, ag8.w, ag9.x, ag9.y, ag9.z, ag9.w};
+            uint32_t Bg[8] = {0, 0, 0, 0, 0, 0, 0, 0}, Bh[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            if (GU) {
+                const uint8_t* U = st + TILE_BYTES;
+                const uint4 au0 = lds128(U + r0 * 128 + c0), au1 = lds128(U + r0 * 128 + c1);
+                const uint4 au8 = lds128(U + (r0 + 8) * 128 + c0), au9 = lds128(U + (r0 + 8) * 128 + c1);
+                Bg[0] = au0.x; Bg[1] = au0.y; Bg[2] = au0.z; Bg[3] = au0.w;
+                Bg[4] = au1.x; Bg[5] = au1.y; Bg[6] = au1.z; Bg[7] = au1.w;
+                Bh[0] = au8.x; Bh[1] = au8.y; Bh[2] = au8.z; Bh[3] = au8.w;
+                Bh[4] = au9.x; Bh[5] = au9.y; Bh[6] = au9.z; Bh[7] = au9.w;
+            }
+#pragma unroll
+            for (int nt = 0; nt < BN / 8; ++nt) {
+                if (nt < nt_active) {
+                    const uint8_t* xr = X + (nt * 8 + g) * XSTRIDE;
+                    const uint4 xb0 = lds128(xr + (2 * q) * 16), xb1 = lds128(xr + (2 * q + 1) * 16);
+                    const uint32_t Bx[8] = {xb0.x, xb0.y, xb0.z, xb0.w, xb1.x, xb1.y, xb1.z, xb1.w};
+                    float pg[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int m = 0; m < 4; ++m)
+                        mma_e4m3_16832(pg, Ag[2 * m], Ah[2 * m], Ag[2 * m + 1], Ah[2 * m + 1], Bx[2 * m],
+                                       Bx[2 * m + 1], pg);
+                    const float s0 = swg * sa[nt][0], s1 = swg * sa[nt][1];
+                    accg[nt][0] = __fmaf_rn(pg[0], s0, accg[nt][0]);
+                    accg[nt][1] = __fmaf_rn(pg[1], s1, accg[nt][1]);
+                    accg[nt][2] = __fmaf_rn(pg[2], s0, accg[nt][2]);
+                    accg[nt][3] = __fmaf_rn(pg[3], s1, accg[nt][3]);
+                    if (GU) {
+                        float pu[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int m = 0; m < 4; ++m)
+                            mma_e4m3_16832(pu, Bg[2 * m], Bh[2 * m], Bg[2 * m + 1], Bh[2 * m + 1], Bx[2 * m],
+                                           Bx[2 * m + 1], pu);
+                        const float t0 = swu * sa[nt][0], t1 = swu * sa[nt][1];
+                        accu[nt][0] = __fmaf_rn(pu[0], t0, accu[nt][0]);
+                        accu[nt][1] = __fmaf_rn(pu[1], t1, accu[nt][1]);
+                        accu[nt][2] = __fmaf_rn(pu[2], t0, accu[nt][2]);
+                        accu[nt][3] = __fmaf_rn(pu[3], t1, accu[nt][3]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
+            if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+
+        if (GU) {
+            // ---------------------------------------------- SiLU(g)*u, 1x128 quantisation
+            uint8_t* qst = epi;                                   // [BN][144] codes
+            float* amax_s = reinterpret_cast<float*>(epi + BN * 144);   // [CW][BN]
+            float h[BN / 8][4];
+#pragma unroll
+            for (int nt = 0; nt < BN / 8; ++nt) {
+                float m0 = 0.f, m1 = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) h[nt][i] = silu_mul(accg[nt][i], accu[nt][i]);
+                m0 = fmaxf(fabsf(h[nt][0]), fabsf(h[nt][2]));
+                m1 = fmaxf(fabsf(h[nt][1]), fabsf(h[nt][3]));
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    m0 = fmaxf(m0, __shfl_xor_sync(0xFFFFFFFFu, m0, off));
+                    m1 = fmaxf(m1, __shfl_xor_sync(0xFFFFFFFFu, m1, off));
+                }
+                if (g == 0) {
+                    amax_s[warp * BN + nt * 8 + 2 * q] = m0;
+                    amax_s[warp * BN + nt * 8 + 2 * q + 1] = m1;
+                }
+            }
+            named_bar_sync(1, CW * 32);
+#pragma unroll
+            for (int nt = 0; nt < BN / 8; ++nt) {
+                if (nt < nt_active) {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int col = nt * 8 + 2 * q + j;
+                        float am = 0.f;
+#pragma unroll
+                        for (int w2 = 0; w2 < CW; ++w2) am = fmaxf(am, amax_s[w2 * BN + col]);
+                        const float sc = (am > 0.f) ? __fdiv_rn(am, 448.0f) : 1.0f;
+                        const uint16_t pq = f32x2_to_e4m3x2(__fdiv_rn(h[nt][j], sc), __fdiv_rn(h[nt][2 + j], sc));
+                        qst[col * 144 + r0] = (uint8_t)(pq & 0xFF);
+                        qst[col * 144 + r0 + 8] = (uint8_t)(pq >> 8);
+                        if (warp == 0 && g == 0 && col < un.valid)
+                            a.shT[(size_t)un.mb * a.ld + un.row_begin + col] = sc;
+                    }
+                }
+            }
+            named_bar_sync(1, CW * 32);
+            // 16 bytes per thread, 8 rows per pass
+            const int tid = threadIdx.x;
+            for (int rr = tid >> 3; rr < un.valid; rr += (CW * 32) >> 3) {
+                const uint4 v = lds128(qst + rr * 144 + (tid & 7) * 16);
+                *reinterpret_cast<uint4*>(a.hq + (size_t)(un.row_begin + rr) * a.M + un.mb * QB + (tid & 7) * 16) = v;
+            }
+            named_bar_sync(1, CW * 32);
+        } else {
+            // ---------------------------------------------- fp32 expert output rows
+            float* ost = reinterpret_cast<float*>(epi);           // [BN][132]
+#pragma unroll
+            for (int nt = 0; nt < BN / 8; ++nt) {
+                if (nt < nt_active) {
+                    const int col = nt * 8 + 2 * q;
+                    ost[col * 132 + r0] = accg[nt][0];
+                    ost[(col + 1) * 132 + r0] = accg[nt][1];
+                    ost[col * 132 + r0 + 8] = accg[nt][2];
+                    ost[(col + 1) * 132 + r0 + 8] = accg[nt][3];
+                }
+            }
+            named_bar_sync(1, CW * 32);
+            const int tid = threadIdx.x;
+            for (int rr = tid >> 5; rr < un.valid; rr += (CW * 32) >> 5) {
+                const float4 v = *reinterpret_cast<const float4*>(ost + rr * 132 + (tid & 31) * 4);
+                *reinterpret_cast<float4*>(a.out + (size_t)(un.row_begin + rr) * a.M + un.mb * QB + (tid & 31) * 4) = v;
+            }
+            named_bar_sync(1, CW * 32);
+        }
+    }
+}
+
+template <bool GU>
+static cudaError_t launch_expert(const moe_layer* L, const WsLayout& lay, char* ws, int max_units, cudaStream_t s) {
+    using C = Cfg<GU>;
+    static bool attr_set[2] = {false, false};
+    if (!attr_set[GU]) {
+        cudaError_t e = cudaFuncSetAttribute(expert_gemm_kernel<GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM + 1024);
+        if (e != cudaSuccess) return e;
+        attr_set[GU] = true;
+    }
+    ExpertArgs a;
+    const int H = L->d.hidden, I = L->d.inter;
+    a.gt = reinterpret_cast<const GroupTable*>(ws + lay.table);
+    a.ld = lay.rows_pad;
+    a.status = L->dev_status;
+    a.wait_limit = L->wait_limit;
+    a.hq = reinterpret_cast<uint8_t*>(ws + lay.hq);
+    a.shT = reinterpret_cast<float*>(ws + lay.shT);
+    a.out = reinterpret_cast<float*>(ws + lay.o);
+    if (GU) {
+        a.w = L->w_gu; a.wscale = L->s_gu;
+        a.act = reinterpret_cast<const uint8_t*>(ws + lay.xp);
+        a.actsT = reinterpret_cast<const float*>(ws + lay.sxT);
+        a.K = H; a.M = I;
+    } else {
+        a.w = L->w_dn; a.wscale = L->s_dn;
+        a.act = reinterpret_cast<const uint8_t*>(ws + lay.hq);
+        a.actsT = reinterpret_cast<const float*>(ws + lay.shT);
+        a.K = I; a.M = H;
+    }
+    int grid = L->num_sms;
+    if (max_units > 0 && max_units < grid) grid = max_units;
+    expert_gemm_kernel<GU><<<grid, NTHREADS, C::SMEM + 1024, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_expert_gate_up(const moe_layer* L, int T, const WsLayout& lay, char* ws, int bn, int max_units,
+                                  cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    if (bn != BN) return cudaErrorInvalidValue;
+    return launch_expert<true>(L, lay, ws, max_units, s);
+}
+
+cudaError_t launch_expert_down(const moe_layer* L, int T, const WsLayout& lay, char* ws, int bn, int max_units,
+                               cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    if (bn != BN) return cudaErrorInvalidValue;
+    return launch_expert<false>(L, lay, ws, max_units, s);
+}
+
+// ---------------------------------------------------------------------------
+// Combine ("weighted reduction" after the experts, SmallEP section of the
+// CPU-GPU hybrid inference article): per token, in this fixed order,
+//   y = O[shared row] + w_0 O[row_0] + ... + w_{k-1} O[row_{k-1}]
+// in fp32, rounded once to bf16.  One CTA per token, 4 channels per thread
+// per step.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ O, const int32_t* __restrict__ inv_row,
+                                                      const float* __restrict__ w, const int32_t* __restrict__ offsets,
+                                                      int T, int H, int k, int E, int n_shared,
+                                                      uint16_t* __restrict__ y) {
+    __shared__ int rows[MAX_TOPK];
+    __shared__ float wt[MAX_TOPK];
+    const int t = blockIdx.x;
+    if (threadIdx.x < k) {
+        rows[threadIdx.x] = inv_row[(size_t)t * k + threadIdx.x];
+        wt[threadIdx.x] = w[(size_t)t * k + threadIdx.x];
+    }
+    __syncthreads();
+    const size_t shrow = (size_t)offsets[E] + t;
+    for (int c = threadIdx.x * 4; c < H; c += blockDim.x * 4) {
+        float4 acc = n_shared ? *reinterpret_cast<const float4*>(O + shrow * H + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < k; ++j) {
+            const float4 o = *reinterpret_cast<const float4*>(O + (size_t)rows[j] * H + c);
+            const float wj = wt[j];
+            acc.x = __fmaf_rn(wj, o.x, acc.x);
+            acc.y = __fmaf_rn(wj, o.y, acc.y);
+            acc.z = __fmaf_rn(wj, o.z, acc.z);
+            acc.w = __fmaf_rn(wj, o.w, acc.w);
+        }
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 pk;
+        pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(y + (size_t)t * H + c) = pk;
+    }
+}
+
+cudaError_t launch_combine(const moe_layer* L, int T, const WsLayout& lay, char* ws, uint16_t* y, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    combine_kernel<<<T, 256, 0, s>>>(reinterpret_cast<const float*>(ws + lay.o),
+                                     reinterpret_cast<const int32_t*>(ws + lay.inv_row),
+                                     reinterpret_cast<const float*>(ws + lay.w),
+                                     reinterpret_cast<const int32_t*>(ws + lay.offsets), T, L->d.hidden, L->d.top_k,
+                                     L->d.n_experts, L->d.n_shared, y);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Weight repacking at load time (KTransformers deep dive, section 2.2:
+// expert weights are laid out once for the compute unit).  Checkpoint
+// [G][R][C] row-major codes -> tile images (see moe_internal.cuh); gate and
+// up interleaved per (row block, k block).  One thread per 16-byte chunk.
+// ---------------------------------------------------------------------------
+__global__ void repack_kernel(const uint8_t* __restrict__ src0, const uint8_t* __restrict__ src1, int n_mat_per_tile,
+                              int G, int R, int C, uint8_t* __restrict__ dst) {
+    const size_t n_chunks = (size_t)G * R * C / 16 * n_mat_per_tile;
+    const int RB = R / QB, CB = C / QB;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n_chunks; i += (size_t)gridDim.x * blockDim.x) {
+        size_t rem = i;
+        const int cpos = rem % 8; rem /= 8;
+        const int r = rem % QB; rem /= QB;
+        const int mat = rem % n_mat_per_tile; rem /= n_mat_per_tile;
+        const int cb = rem % CB; rem /= CB;
+        const int rb = rem % RB; rem /= RB;
+        const int gidx = (int)rem;
+        const int c = cpos ^ (r & 7);
+        const uint8_t* src = mat ? src1 : src0;
+        const uint4 v = *reinterpret_cast<const uint4*>(src + ((size_t)gidx * R + rb * QB + r) * C + cb * QB + c * 16);
+        *reinterpret_cast<uint4*>(dst + i * 16) = v;
+    }
+}
+
+__global__ void repack_scales_kernel(const float* __restrict__ s0, const float* __restrict__ s1, int n_mat, size_t n,
+                                     float* __restrict__ dst) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        dst[i * n_mat] = s0[i];
+        if (n_mat == 2) dst[i * 2 + 1] = s1[i];
+    }
+}
+
+cudaError_t launch_repack(const moe_layer* L, const moe_weights* w, cudaStream_t s) {
+    const int H = L->d.hidden, I = L->d.inter, E = L->d.n_experts;
+    const size_t gu_per = (size_t)I * H * 2, dn_per = (size_t)H * I;
+    const size_t sgu_per = (size_t)(I / QB) * (H / QB) * 2, sdn_per = (size_t)(H / QB) * (I / QB);
+    const int threads = 256, blocks = 4 * L->num_sms;
+    repack_kernel<<<blocks, threads, 0, s>>>(w->w_gate, w->w_up, 2, E, I, H, L->w_gu);
+    repack_kernel<<<blocks, threads, 0, s>>>(w->w_down, w->w_down, 1, E, H, I, L->w_dn);
+    repack_scales_kernel<<<blocks, threads, 0, s>>>(w->s_gate, w->s_up, 2, (size_t)E * (I / QB) * (H / QB), L->s_gu);
+    repack_scales_kernel<<<blocks, threads, 0, s>>>(w->s_down, w->s_down, 1, (size_t)E * (H / QB) * (I / QB), L->s_dn);
+    if (L->d.n_shared) {
+        repack_kernel<<<blocks, threads, 0, s>>>(w->sh_gate, w->sh_up, 2, 1, I, H, L->w_gu + (size_t)E * gu_per);
+        repack_kernel<<<blocks, threads, 0, s>>>(w->sh_down, w->sh_down, 1, 1, H, I, L->w_dn + (size_t)E * dn_per);
+        repack_scales_kernel<<<blocks, threads, 0, s>>>(w->sh_s_gate, w->sh_s_up, 2, (size_t)(I / QB) * (H / QB),
+                                                        L->s_gu + (size_t)E * sgu_per);
+        repack_scales_kernel<<<blocks, threads, 0, s>>>(w->sh_s_down, w->sh_s_down, 1, (size_t)(H / QB) * (I / QB),
+                                                        L->s_dn + (size_t)E * sdn_per);
+    }
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// A bounded wait on an mbarrier nobody signals: exercises the timeout path
+// (status bit set, kernel returns) without hanging or faulting.
+// ---------------------------------------------------------------------------
+__global__ void timeout_probe_kernel(uint32_t* status, uint32_t limit) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        mbar_wait_bounded(&bar, 0, limit, status, nullptr);
+    }
+}
+
+cudaError_t launch_timeout_probe(const moe_layer* L, cudaStream_t s) {
+    timeout_probe_kernel<<<1, 32, 0, s>>>(L->dev_status, L->wait_limit);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

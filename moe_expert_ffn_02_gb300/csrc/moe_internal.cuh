@@ -1,0 +1,217 @@
+// Internal definitions shared by the kernels and the C-ABI layer of the
+// GB300 (sm_103a) MoE FFN library.  Nothing here is part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int QB = 128;               // quantisation / scale block edge
+constexpr int TILE_BYTES = QB * QB;   // one 128x128 FP8 weight tile image
+constexpr int MAX_TOPK = 32;
+constexpr int MAX_EXPERTS = 1024;
+constexpr int ROW_PAD = 128;          // spare rows after every permuted buffer
+
+// ---------------------------------------------------------------------------
+// Weight tile image.  A [R][C] FP8 matrix (C contiguous) is stored as tiles
+// [R/128][C/128] of 16 KB; inside a tile, row r (0..127) occupies bytes
+// [128 r, 128 r + 128) and its 16-byte chunk c is stored at chunk position
+// c ^ (r & 7).  This is the K-major, 128-byte-swizzled operand layout of the
+// Blackwell tensor-core descriptors (8-row x 128 B swizzle atoms stacked
+// along the rows every 1024 B), so a tile can be moved into shared memory by
+// one bulk copy and consumed as is.  Gate and up tiles of the same
+// (row block, k block) sit next to each other (32 KB), gate first.
+// ---------------------------------------------------------------------------
+__host__ __device__ inline int swz_chunk(int r, int c) { return c ^ (r & 7); }
+
+// Per-group work description built on the device from the routing.
+// A "group" is one expert with at least one row (the shared expert is
+// group expert = E with rows R..R+T-1).  Units of the expert GEMMs are
+// (group, n tile of BN rows, m tile of 128 outputs), m fastest.
+struct GroupTable {
+    int32_t n_groups;
+    int32_t n_pairs;        // sum over groups of ceil(rows / bn)
+    int32_t bn;             // n-tile height used to build the table
+    int32_t total_rows;     // R + T (rows of the permuted buffers)
+    int32_t expert[MAX_EXPERTS + 1];
+    int32_t row0[MAX_EXPERTS + 1];
+    int32_t rows[MAX_EXPERTS + 1];
+    int32_t pair_start[MAX_EXPERTS + 2];
+};
+
+// Workspace carve-up for one call (all offsets 256-byte aligned).
+struct WsLayout {
+    size_t logit_part;   // f32 [ksplit][T][E] router partial sums
+    size_t logits;       // f32 [T][E]
+    size_t ids;          // i32 [T][k]
+    size_t w;            // f32 [T][k]
+    size_t chunk_cnt;    // i32 [n_chunks][E]
+    size_t chunk_base;   // i32 [n_chunks][E]
+    size_t offsets;      // i32 [E+1]
+    size_t sorted_tok;   // i32 [T*k]
+    size_t inv_row;      // i32 [T][k]
+    size_t table;        // GroupTable
+    size_t xp;           // u8  [rows+pad][H]   permuted quantised x
+    size_t sxT;          // f32 [H/128][rows+pad]
+    size_t hq;           // u8  [rows+pad][I]   quantised h
+    size_t shT;          // f32 [I/128][rows+pad]
+    size_t o;            // f32 [rows][H]       expert outputs (unweighted)
+    size_t total;
+    int ksplit, n_chunks, rows_pad;
+};
+
+constexpr int CHUNK_TOK = 64;         // tokens per permutation chunk (one warp)
+
+}  // namespace moe
+
+struct moe_layer {
+    moe_desc d;
+    int device;
+    int num_sms;
+    int n_groups_max;      // E + n_shared
+    uint8_t* w_gu;         // [G][I/128][H/128][2][16 KB] gate/up tile images
+    uint8_t* w_dn;         // [G][H/128][I/128][16 KB]    down tile images
+    float* s_gu;           // [G][I/128][H/128][2]
+    float* s_dn;           // [G][H/128][I/128]
+    float* router_w;       // [E][H]
+    float* router_b;       // [E] (zeros when no bias)
+    uint32_t* dev_status;  // device status word
+    uint32_t wait_limit;
+    bool profile;          // record stage events in forward calls
+    cudaEvent_t ev[MOE_PROFILE_STAGES + 1];
+    cudaStream_t ev_stream;
+};
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Device helpers (PTX wrappers).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait: gives up after `limit_us` microseconds of wall time, or as
+// soon as another thread of the CTA has given up (*abort != 0).  On expiry
+// it sets the timeout bit of the device status word and *abort, and returns
+// false; the caller then abandons its work.  Nothing traps.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t limit_us,
+                                                  uint32_t* status, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (abort && *abort) return false;
+        if ((i & 63u) == 0 && global_ns() - t0 > (uint64_t)limit_us * 1000ull) {
+            atomicOr(status, MOE_DEV_WAIT_TIMEOUT);
+            if (abort) *abort = 1;
+            return false;
+        }
+    }
+}
+
+// 1-D bulk copy global -> shared, completion counted on an mbarrier.
+// src, dst 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(const void* p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_addr(p)));
+    return v;
+}
+
+// D = A(16x32 e4m3, row) * B(32x8 e4m3, col) + C, fp32 accumulate.
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1, const float (&c)[4]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+}
+
+// Two fp32 -> two E4M3FN (round to nearest even, saturate to +-448);
+// `lo` lands in the low byte.
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d) {
+    return (uint32_t)f32x2_to_e4m3x2(a, b) | ((uint32_t)f32x2_to_e4m3x2(c, d) << 16);
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+}  // namespace moe
+
+// Launchers (defined in the .cu files, called from api.cu).
+namespace moe {
+cudaError_t launch_repack(const moe_layer* L, const moe_weights* w, cudaStream_t s);
+cudaError_t launch_router_logits(const moe_layer* L, const uint16_t* x, int T, float* part, int ksplit,
+                                 cudaStream_t s);
+cudaError_t launch_topk(const moe_layer* L, const float* part, int ksplit, bool add_bias, int T, float* logits_out,
+                        int32_t* ids, float* w, cudaStream_t s);
+cudaError_t launch_permute(const moe_layer* L, const int32_t* ids, int T, const WsLayout& lay, char* ws, int bn,
+                           int32_t* offsets_out, int32_t* sorted_out, int32_t* inv_out, cudaStream_t s);
+cudaError_t launch_quant_scatter(const moe_layer* L, const uint16_t* x, int T, const WsLayout& lay, char* ws,
+                                 uint8_t* xq_out, float* sx_out, cudaStream_t s);
+cudaError_t launch_expert_gate_up(const moe_layer* L, int T, const WsLayout& lay, char* ws, int bn, int max_units,
+                                  cudaStream_t s);
+cudaError_t launch_expert_down(const moe_layer* L, int T, const WsLayout& lay, char* ws, int bn, int max_units,
+                               cudaStream_t s);
+cudaError_t launch_combine(const moe_layer* L, int T, const WsLayout& lay, char* ws, uint16_t* y, cudaStream_t s);
+cudaError_t launch_timeout_probe(const moe_layer* L, cudaStream_t s);
+}  // namespace moe

@@ -1,0 +1,493 @@
+// Routing stage of the MoE layer on sm_103a: router logits, top-k with gate
+// weights, expert grouping (histogram -> scan -> stable scatter) and the
+// 1x128 E4M3 quantisation of x written straight into the grouped rows.
+//
+// Sources: "KTransformers deep dive" (chenxutan.com), section 1.2 (router
+// picks 8 of 256 experts plus a shared one) and section 2.2 (tokens of one
+// expert are batched so GEMV becomes GEMM); CPU-GPU hybrid inference article
+// (xingyun.xin), SmallEP section / Fig. 5 (gating and sorting come before
+// dispatch).  Scoring = softmax over the selected logits (renormalised
+// top-k), ties to the lower expert index.
+#include "moe_internal.cuh"
+
+#include <math_constants.h>
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Router logits: part[z][t][e] = sum_{h in split z} x[t][h] * Wr[e][h]
+// (fp32 FMA; each 32-wide K step is summed into a fresh partial before it is
+// added to the running total, which keeps the rounding error near
+// sqrt(H/32) ulp).  The bias and the sum over splits are added by the top-k
+// kernel in a fixed order.  Tile: 64 tokens x 64 experts per CTA, 4x4 per
+// thread; split z covers H/ksplit consecutive channels (grid.z = ksplit, so
+// a decode batch still spreads the router weights over >= 152 CTAs).
+// ---------------------------------------------------------------------------
+constexpr int LT = 64, LE = 64, LK = 32;
+
+__global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __restrict__ x,
+                                                            const float* __restrict__ W, int T, int H, int E,
+                                                            int kchunk, float* __restrict__ part) {
+    __shared__ float xs[LK][LT + 4];
+    __shared__ float ws[LK][LE + 4];
+    const int tid = threadIdx.x;
+    const int tx = tid & 15, ty = tid >> 4;
+    const int t0 = blockIdx.y * LT, e0 = blockIdx.x * LE;
+    const int z = blockIdx.z;
+    const int kbeg = z * kchunk, kend = kbeg + kchunk;
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+
+    const int lr = tid >> 2;          // row (token / expert) this thread loads
+    const int lc = (tid & 3) * 8;     // 8 consecutive channels
+    for (int k0 = kbeg; k0 < kend; k0 += LK) {
+        {
+            const int t = t0 + lr;
+            float v[8];
+            if (t < T) {
+                uint4 raw = *reinterpret_cast<const uint4*>(x + (size_t)t * H + k0 + lc);
+                const uint32_t wds[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    v[2 * i] = __uint_as_float(wds[i] << 16);
+                    v[2 * i + 1] = __uint_as_float(wds[i] & 0xFFFF0000u);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) xs[lc + i][lr] = v[i];
+        }
+        {
+            const int e = e0 + lr;
+            float v[8];
+            if (e < E) {
+                const float4* src = reinterpret_cast<const float4*>(W + (size_t)e * H + k0 + lc);
+                float4 a = src[0], b = src[1];
+                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+                v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ws[lc + i][lr] = v[i];
+        }
+        __syncthreads();
+        float p[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) p[i][j] = 0.f;
+#pragma unroll 8
+        for (int kk = 0; kk < LK; ++kk) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = xs[kk][ty * 4 + i];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) b[j] = ws[kk][tx * 4 + j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) p[i][j] = __fmaf_rn(a[i], b[j], p[i][j]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = __fadd_rn(acc[i][j], p[i][j]);
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int t = t0 + ty * 4 + i;
+        if (t >= T) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int e = e0 + tx * 4 + j;
+            if (e < E) part[((size_t)z * T + t) * E + e] = acc[i][j];
+        }
+    }
+}
+
+cudaError_t launch_router_logits(const moe_layer* L, const uint16_t* x, int T, float* part, int ksplit,
+                                 cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    const int H = L->d.hidden, E = L->d.n_experts;
+    dim3 grid((E + LE - 1) / LE, (T + LT - 1) / LT, ksplit);
+    router_logits_kernel<<<grid, 256, 0, s>>>(x, L->router_w, T, H, E, H / ksplit, part);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// exp in fp32 for the gate weights: Cody & Waite reduction x = n ln2 + r
+// (ln2 split into a 15-significant-bit head, so n * head is exact for
+// |n| < 512, and a tail), degree-7 Taylor polynomial of e^r on
+// |r| <= ln2/2 by Horner's rule with fused multiply-adds, exact scaling by
+// 2^n.  Arguments below -86 give 0 (keeps 2^n a normal number).  Every
+// operation is an explicitly rounded fp32 intrinsic, so the result is fully
+// determined by the argument.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float gate_exp(float x) {
+    const float log2e = (float)1.4426950408889634;
+    const float ln2_hi = 0x1.62e4p-1f;
+    const float ln2_lo = (float)(0.69314718055994530942 - 0.693145751953125);
+    const float c2 = (float)(1.0 / 2.0), c3 = (float)(1.0 / 6.0);
+    const float c4 = (float)(1.0 / 24.0), c5 = (float)(1.0 / 120.0);
+    const float c6 = (float)(1.0 / 720.0), c7 = (float)(1.0 / 5040.0);
+    if (!(x >= -86.0f)) return 0.0f;
+    if (x > 88.0f) return CUDART_INF_F;
+    const float n = rintf(__fmul_rn(x, log2e));
+    float r = __fmaf_rn(-n, ln2_hi, x);
+    r = __fmaf_rn(-n, ln2_lo, r);
+    float p = c7;
+    p = __fmaf_rn(p, r, c6);
+    p = __fmaf_rn(p, r, c5);
+    p = __fmaf_rn(p, r, c4);
+    p = __fmaf_rn(p, r, c3);
+    p = __fmaf_rn(p, r, c2);
+    p = __fmaf_rn(p, r, 1.0f);
+    p = __fmaf_rn(p, r, 1.0f);
+    const float two_n = __int_as_float(((int)n + 127) << 23);
+    return __fmul_rn(p, two_n);
+}
+
+// ---------------------------------------------------------------------------
+// Top-k + gate weights, one warp per token.  Lane l holds experts
+// l, l+32, ...; each of the k rounds takes the warp-wide maximum of the
+// remaining logits, larger value first and lower index on ties (-0 == +0).
+// Weights: m = L[id0]; e_j = exp(L[id_j] - m); S = e_0 + e_1 + ... summed
+// left to right; w_j = e_j / S -- each step an IEEE-rounded fp32 op.
+// ---------------------------------------------------------------------------
+template <int PER>
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ part, int ksplit,
+                                                   const float* __restrict__ bias, int T, int E, int k,
+                                                   float* __restrict__ logits_out, int32_t* __restrict__ ids,
+                                                   float* __restrict__ wout) {
+    __shared__ float sel_v[8][MAX_TOPK];
+    __shared__ int sel_i[8][MAX_TOPK];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= T) return;
+    float v[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) {
+            float acc = part[(size_t)t * E + e];
+            for (int z = 1; z < ksplit; ++z) acc = __fadd_rn(acc, part[((size_t)z * T + t) * E + e]);
+            if (bias) acc = __fadd_rn(acc, bias[e]);
+            v[i] = acc;
+            if (logits_out) logits_out[(size_t)t * E + e] = acc;
+        } else {
+            v[i] = -CUDART_INF_F;
+        }
+    }
+    uint32_t taken = 0;
+    for (int j = 0; j < k; ++j) {
+        float bv = -CUDART_INF_F;
+        int bi = 0x7FFFFFFF;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E && !((taken >> i) & 1u)) {
+                if (bi == 0x7FFFFFFF || v[i] > bv) { bv = v[i]; bi = e; }
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
+            const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
+            const bool better = (oi != 0x7FFFFFFF) &&
+                                (bi == 0x7FFFFFFF || ov > bv || (ov == bv && oi < bi));
+            if (better) { bv = ov; bi = oi; }
+        }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (lane == 0) { sel_v[warp][j] = bv; sel_i[warp][j] = bi; }
+    }
+    __syncwarp();
+    if (lane == 0) {
+        const float m = sel_v[warp][0];
+        float ev[MAX_TOPK];
+        float S = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            ev[j] = gate_exp(__fsub_rn(sel_v[warp][j], m));
+            S = (j == 0) ? ev[0] : __fadd_rn(S, ev[j]);
+        }
+        for (int j = 0; j < k; ++j) {
+            if (ids) ids[(size_t)t * k + j] = sel_i[warp][j];
+            if (wout) wout[(size_t)t * k + j] = __fdiv_rn(ev[j], S);
+        }
+    }
+}
+
+cudaError_t launch_topk(const moe_layer* L, const float* part, int ksplit, bool add_bias, int T, float* logits_out,
+                        int32_t* ids, float* w, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    const int E = L->d.n_experts, k = L->d.top_k;
+    const float* bias = add_bias ? L->router_b : nullptr;
+    const int per = (E + 31) / 32;
+    dim3 grid((T + 7) / 8);
+#define MOE_TOPK_CASE(P)                                                                              \
+    if (per <= P) {                                                                                   \
+        topk_kernel<P><<<grid, 256, 0, s>>>(part, ksplit, bias, T, E, k, logits_out, ids, w);         \
+        return cudaGetLastError();                                                                    \
+    }
+    MOE_TOPK_CASE(1) MOE_TOPK_CASE(2) MOE_TOPK_CASE(4) MOE_TOPK_CASE(8) MOE_TOPK_CASE(12)
+    MOE_TOPK_CASE(16) MOE_TOPK_CASE(24) MOE_TOPK_CASE(32)
+#undef MOE_TOPK_CASE
+    return cudaErrorInvalidValue;
+}
+
+// ---------------------------------------------------------------------------
+// Expert grouping.  The (token, slot) pairs are cut into chunks of
+// CHUNK_TOK tokens, one warp each.
+//   count:   per chunk, per expert, how many pairs chose it;
+//   scan:    one CTA turns the counts into the expert offsets (exclusive
+//            prefix sum over experts) and, for every chunk, the first row
+//            its pairs of expert e will take; it also builds the group
+//            table the expert GEMMs iterate over;
+//   scatter: each warp walks its chunk in token-major order, 32 pairs at a
+//            time, ranks equal experts with a warp match, and writes
+//            sorted_token / inv_row.  Rows inside an expert therefore
+//            ascend with the token index, independent of scheduling.
+// Ids outside [0, E) set MOE_DEV_BAD_EXPERT_ID and are clamped so that
+// every later access stays in bounds.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int clamp_expert(int e, int E, uint32_t* status) {
+    if (e < 0 || e >= E) {
+        atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
+        e = e < 0 ? 0 : E - 1;
+    }
+    return e;
+}
+
+__global__ void __launch_bounds__(128) perm_count_kernel(const int32_t* __restrict__ ids, int T, int E, int k,
+                                                         int n_chunks, int32_t* __restrict__ chunk_cnt,
+                                                         uint32_t* status) {
+    extern __shared__ int32_t cnt_smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x * 4 + warp;
+    if (c >= n_chunks) return;
+    int32_t* cnt = cnt_smem + warp * E;
+    for (int e = lane; e < E; e += 32) cnt[e] = 0;
+    __syncwarp();
+    const int t0 = c * CHUNK_TOK;
+    const int t1 = min(T, t0 + CHUNK_TOK);
+    const int n = (t1 - t0) * k;
+    for (int i = lane; i < n; i += 32) {
+        const int e = clamp_expert(ids[(size_t)t0 * k + i], E, status);
+        atomicAdd(&cnt[e], 1);
+    }
+    __syncwarp();
+    for (int e = lane; e < E; e += 32) chunk_cnt[(size_t)c * E + e] = cnt[e];
+}
+
+// Exclusive scan across a 1024-thread block; returns this thread's prefix
+// and writes the block total to *total.
+__device__ int block_excl_scan_1024(int v, int* total) {
+    __shared__ int warp_sums[32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int ws = warp_sums[lane];
+        int wi = ws;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xFFFFFFFFu, wi, off);
+            if (lane >= off) wi += o;
+        }
+        warp_sums[lane] = wi - ws;
+        if (lane == 31) *total = wi;
+    }
+    __syncthreads();
+    const int r = warp_sums[warp] + incl - v;
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(1024) perm_scan_kernel(const int32_t* __restrict__ chunk_cnt, int n_chunks, int T,
+                                                         int E, int k, int n_shared, int bn,
+                                                         int32_t* __restrict__ chunk_base,
+                                                         int32_t* __restrict__ offsets,
+                                                         int32_t* __restrict__ offsets_out, GroupTable* gt) {
+    __shared__ int total_s;
+    const int e = threadIdx.x;
+    int tot = 0;
+    if (e < E) {
+        for (int c = 0; c < n_chunks; ++c) {
+            const int v = chunk_cnt[(size_t)c * E + e];
+            chunk_base[(size_t)c * E + e] = tot;
+            tot += v;
+        }
+    }
+    const int off = block_excl_scan_1024(e < E ? tot : 0, &total_s);
+    const int R = total_s;
+    if (e < E) {
+        offsets[e] = off;
+        if (offsets_out) offsets_out[e] = off;
+        for (int c = 0; c < n_chunks; ++c) chunk_base[(size_t)c * E + e] += off;
+    }
+    if (e == 0) {
+        offsets[E] = R;
+        if (offsets_out) offsets_out[E] = R;
+    }
+    // group table: active experts in index order, then the shared expert
+    const bool active = (e < E) && tot > 0;
+    const int gidx = block_excl_scan_1024(active ? 1 : 0, &total_s);
+    const int n_routed = total_s;
+    const int tiles = active ? (tot + bn - 1) / bn : 0;
+    const int pstart = block_excl_scan_1024(tiles, &total_s);
+    const int routed_pairs = total_s;
+    if (active) {
+        gt->expert[gidx] = e;
+        gt->row0[gidx] = off;
+        gt->rows[gidx] = tot;
+        gt->pair_start[gidx] = pstart;
+    }
+    if (e == 0) {
+        int ng = n_routed, np = routed_pairs;
+        if (n_shared && T > 0) {
+            gt->expert[ng] = E;
+            gt->row0[ng] = R;
+            gt->rows[ng] = T;
+            gt->pair_start[ng] = np;
+            np += (T + bn - 1) / bn;
+            ng += 1;
+        }
+        gt->pair_start[ng] = np;
+        gt->n_groups = ng;
+        gt->n_pairs = np;
+        gt->bn = bn;
+        gt->total_rows = R + (n_shared ? T : 0);
+    }
+}
+
+__global__ void __launch_bounds__(128) perm_scatter_kernel(const int32_t* __restrict__ ids, int T, int E, int k,
+                                                           int n_chunks, const int32_t* __restrict__ chunk_base,
+                                                           int32_t* __restrict__ sorted_token,
+                                                           int32_t* __restrict__ inv_row, uint32_t* status) {
+    extern __shared__ int32_t run_smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x * 4 + warp;
+    if (c >= n_chunks) return;
+    int32_t* run = run_smem + warp * E;
+    for (int e = lane; e < E; e += 32) run[e] = 0;
+    __syncwarp();
+    const int t0 = c * CHUNK_TOK;
+    const int t1 = min(T, t0 + CHUNK_TOK);
+    const int n = (t1 - t0) * k;
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    for (int b = 0; b < n; b += 32) {
+        const int i = b + lane;
+        const bool valid = i < n;
+        int e = valid ? clamp_expert(ids[(size_t)t0 * k + i], E, status) : -1 - lane;
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, e);
+        const int rank = __popc(peers & lt_mask);
+        if (valid) {
+            const int row = chunk_base[(size_t)c * E + e] + run[e] + rank;
+            const int t = t0 + i / k;
+            if (sorted_token) sorted_token[row] = t;
+            inv_row[(size_t)t0 * k + i] = row;
+        }
+        __syncwarp();
+        if (valid && (peers & lt_mask) == 0) run[e] += __popc(peers);
+        __syncwarp();
+    }
+}
+
+cudaError_t launch_permute(const moe_layer* L, const int32_t* ids, int T, const WsLayout& lay, char* ws, int bn,
+                           int32_t* offsets_out, int32_t* sorted_out, int32_t* inv_out, cudaStream_t s) {
+    const int E = L->d.n_experts, k = L->d.top_k;
+    int32_t* chunk_cnt = reinterpret_cast<int32_t*>(ws + lay.chunk_cnt);
+    int32_t* chunk_base = reinterpret_cast<int32_t*>(ws + lay.chunk_base);
+    int32_t* offsets = reinterpret_cast<int32_t*>(ws + lay.offsets);
+    int32_t* sorted_token = sorted_out;   // only the caller needs it
+    int32_t* inv_row = reinterpret_cast<int32_t*>(ws + lay.inv_row);
+    GroupTable* gt = reinterpret_cast<GroupTable*>(ws + lay.table);
+    const int nc = lay.n_chunks;
+    const size_t smem = 4 * E * sizeof(int32_t);
+    if (nc > 0) {
+        perm_count_kernel<<<(nc + 3) / 4, 128, smem, s>>>(ids, T, E, k, nc, chunk_cnt, L->dev_status);
+        cudaError_t err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+    }
+    perm_scan_kernel<<<1, 1024, 0, s>>>(chunk_cnt, nc, T, E, k, L->d.n_shared, bn, chunk_base, offsets, offsets_out,
+                                        gt);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    if (nc > 0) {
+        perm_scatter_kernel<<<(nc + 3) / 4, 128, smem, s>>>(ids, T, E, k, nc, chunk_base, sorted_token, inv_row,
+                                                            L->dev_status);
+        err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+        if (inv_out)
+            err = cudaMemcpyAsync(inv_out, inv_row, sizeof(int32_t) * (size_t)T * k, cudaMemcpyDeviceToDevice, s);
+    }
+    return err;
+}
+
+// ---------------------------------------------------------------------------
+// 1x128 quantisation of x, written to every row the token owns.
+// Per token t and 128-channel group g: amax = max |x|; s = amax / 448
+// (s = 1 if amax = 0); q = E4M3FN(fp32(x / s)) rounded to nearest even with
+// saturation.  Destination rows: inv_row[t][0..k-1] (routed groups) and
+// R + t (shared group).  Scales are stored transposed, sxT[g][row], so a
+// tile of rows reads a contiguous run.  One CTA per token, one warp per
+// group at a time, 4 channels per lane.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __restrict__ x, int T, int H, int k,
+                                                            int n_shared, const int32_t* __restrict__ inv_row,
+                                                            const int32_t* __restrict__ offsets, int E,
+                                                            uint8_t* __restrict__ xp, float* __restrict__ sxT,
+                                                            int ld, uint8_t* __restrict__ xq_out,
+                                                            float* __restrict__ sx_out) {
+    __shared__ int dest[MAX_TOPK + 1];
+    const int t = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nd = k + (n_shared ? 1 : 0);
+    if (threadIdx.x < k) dest[threadIdx.x] = inv_row[(size_t)t * k + threadIdx.x];
+    if (threadIdx.x == 0 && n_shared) dest[k] = offsets[E] + t;
+    __syncthreads();
+    const int G = H / QB;
+    for (int g = warp; g < G; g += 8) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(x + (size_t)t * H + g * QB + lane * 4);
+        const float v0 = __uint_as_float(raw.x << 16), v1 = __uint_as_float(raw.x & 0xFFFF0000u);
+        const float v2 = __uint_as_float(raw.y << 16), v3 = __uint_as_float(raw.y & 0xFFFF0000u);
+        float a = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
+        const float sc = (a > 0.f) ? __fdiv_rn(a, 448.0f) : 1.0f;
+        const uint32_t q = pack4_e4m3(__fdiv_rn(v0, sc), __fdiv_rn(v1, sc), __fdiv_rn(v2, sc), __fdiv_rn(v3, sc));
+        for (int d = 0; d < nd; ++d) {
+            const int row = dest[d];
+            *reinterpret_cast<uint32_t*>(xp + (size_t)row * H + g * QB + lane * 4) = q;
+            if (lane == 0) sxT[(size_t)g * ld + row] = sc;
+        }
+        if (xq_out) *reinterpret_cast<uint32_t*>(xq_out + (size_t)t * H + g * QB + lane * 4) = q;
+        if (sx_out && lane == 0) sx_out[(size_t)t * G + g] = sc;
+    }
+}
+
+cudaError_t launch_quant_scatter(const moe_layer* L, const uint16_t* x, int T, const WsLayout& lay, char* ws,
+                                 uint8_t* xq_out, float* sx_out, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    quant_scatter_kernel<<<T, 256, 0, s>>>(x, T, L->d.hidden, L->d.top_k, L->d.n_shared,
+                                           reinterpret_cast<const int32_t*>(ws + lay.inv_row),
+                                           reinterpret_cast<const int32_t*>(ws + lay.offsets), L->d.n_experts,
+                                           reinterpret_cast<uint8_t*>(ws + lay.xp),
+                                           reinterpret_cast<float*>(ws + lay.sxT), lay.rows_pad, xq_out, sx_out);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,130 @@
+"""Shared helpers for the GPU tests: upload seeded inputs, run the library
+through its C ABI, and compare with the CPU oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import moe_expert_ffn_02_gb300 as moe
+import oracle
+import synth
+
+WEIGHT_KEYS = ("router_w", "router_b", "w_gate", "w_up", "w_down", "s_gate", "s_up", "s_down",
+               "sh_gate", "sh_up", "sh_down", "sh_s_gate", "sh_s_up", "sh_s_down")
+
+
+def to_dev(a):
+    if a is None:
+        return None
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def make_layer(wl: synth.Workload, inp: dict) -> moe.Layer:
+    dev = {k: to_dev(inp.get(k)) for k in WEIGHT_KEYS}
+    layer = moe.Layer(wl.hidden, wl.inter, wl.n_experts, wl.top_k, dev, n_shared=wl.n_shared)
+    del dev
+    return layer
+
+
+def run_forward(layer: moe.Layer, x_bits: np.ndarray, mode: int, want_dbg: bool = True):
+    """x_bits: uint16 [T][H].  Returns (y uint16 [T][H], dbg dict of numpy)."""
+    T, H = x_bits.shape
+    E, k = layer.desc.n_experts, layer.desc.top_k
+    x = to_dev(x_bits.view(np.int16))
+    y = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    dbg = None
+    bufs = {}
+    if want_dbg:
+        bufs = {
+            "topk_ids": torch.empty((T, k), dtype=torch.int32, device="cuda"),
+            "topk_w": torch.empty((T, k), dtype=torch.float32, device="cuda"),
+            "expert_offsets": torch.empty((E + 1,), dtype=torch.int32, device="cuda"),
+            "sorted_token": torch.empty((max(T * k, 1),), dtype=torch.int32, device="cuda"),
+            "inv_row": torch.empty((T, k), dtype=torch.int32, device="cuda"),
+            "xq": torch.empty((T, H), dtype=torch.uint8, device="cuda"),
+            "sx": torch.empty((T, H // 128), dtype=torch.float32, device="cuda"),
+        }
+        dbg = {n: t.data_ptr() for n, t in bufs.items()}
+    ws, nbytes = layer.workspace(T, mode)
+    fn = moe.moe_forward_prefill if mode == moe.MODE_PREFILL else moe.moe_forward_decode
+    fn(layer.handle, x.data_ptr() if T else 0, T, y.data_ptr() if T else 0, dbg, ws, nbytes, layer.stream)
+    torch.cuda.synchronize()
+    st, flags = moe.moe_get_device_status(layer.handle, layer.stream)
+    assert st == 0 and flags == 0, f"device status {st} flags {flags:#x}"
+    out = {n: t.cpu().numpy() for n, t in bufs.items()}
+    if "sorted_token" in out:
+        out["sorted_token"] = out["sorted_token"][: T * k]
+    return y.cpu().numpy().view(np.uint16), out
+
+
+def route(layer: moe.Layer, x_bits: np.ndarray):
+    """moe_route: logits and routing outputs as numpy."""
+    T, H = x_bits.shape
+    E, k = layer.desc.n_experts, layer.desc.top_k
+    x = to_dev(x_bits.view(np.int16))
+    bufs = {
+        "logits": torch.empty((T, E), dtype=torch.float32, device="cuda"),
+        "topk_ids": torch.empty((T, k), dtype=torch.int32, device="cuda"),
+        "topk_w": torch.empty((T, k), dtype=torch.float32, device="cuda"),
+        "expert_offsets": torch.empty((E + 1,), dtype=torch.int32, device="cuda"),
+        "sorted_token": torch.empty((max(T * k, 1),), dtype=torch.int32, device="cuda"),
+        "inv_row": torch.empty((T, k), dtype=torch.int32, device="cuda"),
+    }
+    ws, nbytes = layer.workspace(T, moe.MODE_ROUTE)
+    moe.moe_route(layer.handle, x.data_ptr() if T else 0, T, {n: t.data_ptr() for n, t in bufs.items()}, ws, nbytes,
+                  layer.stream)
+    torch.cuda.synchronize()
+    out = {n: t.cpu().numpy() for n, t in bufs.items()}
+    out["sorted_token"] = out["sorted_token"][: T * k]
+    return out
+
+
+def route_from_logits(layer: moe.Layer, L: np.ndarray):
+    T = L.shape[0]
+    E, k = layer.desc.n_experts, layer.desc.top_k
+    Ld = to_dev(L.astype(np.float32))
+    bufs = {
+        "topk_ids": torch.empty((T, k), dtype=torch.int32, device="cuda"),
+        "topk_w": torch.empty((T, k), dtype=torch.float32, device="cuda"),
+        "expert_offsets": torch.empty((E + 1,), dtype=torch.int32, device="cuda"),
+        "sorted_token": torch.empty((max(T * k, 1),), dtype=torch.int32, device="cuda"),
+        "inv_row": torch.empty((T, k), dtype=torch.int32, device="cuda"),
+    }
+    ws, nbytes = layer.workspace(T, moe.MODE_ROUTE)
+    moe.moe_route_from_logits(layer.handle, Ld.data_ptr() if T else 0, T, {n: t.data_ptr() for n, t in bufs.items()},
+                              ws, nbytes, layer.stream)
+    torch.cuda.synchronize()
+    out = {n: t.cpu().numpy() for n, t in bufs.items()}
+    out["sorted_token"] = out["sorted_token"][: T * k]
+    return out
+
+
+def assert_routing_equal(got: dict, ref: dict):
+    assert np.array_equal(got["topk_ids"], ref["ids"]), "top-k ids differ"
+    assert np.array_equal(got["topk_w"].view(np.uint32), ref["w"].view(np.uint32)), "gate weights differ"
+    assert np.array_equal(got["expert_offsets"], ref["offsets"]), "expert offsets differ"
+    assert np.array_equal(got["sorted_token"], ref["sorted_token"]), "sorted_token differs"
+    assert np.array_equal(got["inv_row"], ref["inv_row"]), "inv_row differs"
+
+
+REL_L2_TOL = 5e-3          # relative L2 error of y
+MAX_ABS_TOL = 3e-2         # max abs error / rms(y_oracle)
+
+
+def compare_y(y_gpu: np.ndarray, y_ref: np.ndarray):
+    """Tolerance of the layer output (bf16): rel-L2 <= 5e-3 and max abs
+    error <= 3e-2 * rms(y_ref).  Returns (rel_l2, max_abs/rms)."""
+    a = synth.bf16_to_f32(y_gpu).astype(np.float64)
+    b = synth.bf16_to_f32(y_ref).astype(np.float64)
+    assert np.all(np.isfinite(a)), "non-finite output"
+    rms = np.sqrt(np.mean(b * b))
+    rel = np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30)
+    mx = np.max(np.abs(a - b)) / max(rms, 1e-30) if a.size else 0.0
+    print(f"[parity] rel_l2={rel:.3e} max_abs/rms={mx:.3e} n={a.size}")
+    assert rel <= REL_L2_TOL, f"relative L2 error {rel:.3e} > {REL_L2_TOL}"
+    assert mx <= MAX_ABS_TOL, f"max abs error {mx:.3e} * rms > {MAX_ABS_TOL}"
+    return rel, mx
+
+
+def oracle_y(inp: dict, k: int, ids, w, rows=None):
+    return oracle.forward(inp, k, ids, w, rows=rows)

@@ -1,0 +1,265 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle on
+the same seeded inputs.  Routing, gate weights, grouping and the quantised
+activations are compared bit for bit; the layer output within
+rel-L2 <= 5e-3 and max-abs <= 3e-2 * rms(y_oracle), with the oracle routed
+by the GPU's own fp32 logits."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def h():
+    import _harness
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import moe_expert_ffn_02_gb300 as moe
+    moe.load()       # no fallback: the extension must be present
+    return _harness
+
+
+def small_wl(E, k, H=256, I=256, T=64, n_shared=1, zipf=0.0, name="small"):
+    return synth.Workload(name, T, H, I, E, k, n_shared=n_shared, zipf_s=zipf)
+
+
+# ------------------------------------------------------------------ routing
+
+@pytest.mark.parametrize("E,k,T", [(8, 2, 64), (256, 8, 1), (256, 8, 16), (256, 8, 1000), (384, 8, 333),
+                                   (1024, 32, 70), (5, 5, 7), (64, 6, 0)])
+def test_route_from_logits_bit_exact(h, E, k, T):
+    wl = small_wl(E, k, H=128, I=128, T=T)
+    inp = synth.make_inputs(wl, seed=1)
+    layer = h.make_layer(wl, inp)
+    rng = np.random.default_rng(E + k + T)
+    L = rng.normal(0, 1, (T, E)).astype(np.float32)
+    if T > 3:
+        L[0, :] = 0.75                            # all tied -> ids 0..k-1
+        L[1, : E // 2] = np.float32(-0.5)         # partial ties
+        L[2, 0], L[2, E - 1] = np.float32(-0.0), np.float32(0.0)
+        L[3] = np.round(L[3] * 4) / 4             # many exact ties
+    got = h.route_from_logits(layer, L)
+    ref = oracle.route_from_logits(L, k)
+    h.assert_routing_equal(got, ref)
+    layer.close()
+
+
+def test_router_logits_tolerance_and_routing(h):
+    wl = synth.WORKLOADS["tiny"]
+    inp = synth.make_inputs(wl, seed=0)
+    layer = h.make_layer(wl, inp)
+    got = h.route(layer, inp["x"])
+    Lref = oracle.logits(inp["x"], inp["router_w"], inp["router_b"])
+    assert np.all(np.abs(got["logits"] - Lref) <= 1e-5 * (1 + np.abs(Lref)))
+    h.assert_routing_equal(got, oracle.route_from_logits(got["logits"], wl.top_k))
+    layer.close()
+
+
+# ------------------------------------------------------------------ layer, small shapes
+
+def check_layer(h, wl, inp, mode, seed_rows=None):
+    import moe_expert_ffn_02_gb300 as moe
+    layer = h.make_layer(wl, inp)
+    y, dbg = h.run_forward(layer, inp["x"], mode)
+    r = h.route(layer, inp["x"])
+    ref_route = oracle.route_from_logits(r["logits"], wl.top_k)
+    h.assert_routing_equal(dbg, ref_route)
+    xq, sx = oracle.quant_1x128(synth.bf16_to_f32(inp["x"]))
+    assert np.array_equal(dbg["xq"], xq), "quantised x differs"
+    assert np.array_equal(dbg["sx"].view(np.uint32), sx.view(np.uint32)), "x scales differ"
+    y_ref = oracle.forward(inp, wl.top_k, ref_route["ids"], ref_route["w"])
+    rel, mx = h.compare_y(y, y_ref)
+    layer.close()
+    return rel, mx, y
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_tiny_layer_parity(h, mode):
+    wl = synth.WORKLOADS["tiny"]
+    check_layer(h, wl, synth.make_inputs(wl, seed=0), mode)
+
+
+@pytest.mark.parametrize("T", [1, 3, 17, 64])
+def test_decode_entry_small_batches(h, T):
+    wl = small_wl(16, 4, H=384, I=256, T=T)
+    check_layer(h, wl, synth.make_inputs(wl, seed=5), 2)
+
+
+@pytest.mark.parametrize("T,E,k,zipf,shared", [(300, 8, 2, 0.0, 1), (1000, 32, 4, 1.2, 1), (257, 16, 3, 0.0, 0),
+                                               (129, 4, 4, 0.0, 1)])
+def test_prefill_ragged_and_skewed(h, T, E, k, zipf, shared):
+    """Several 64-row tiles per expert, ragged tails, empty experts (Zipf
+    bias), no shared expert, and k = E (every token picks every expert)."""
+    wl = small_wl(E, k, H=512, I=384, T=T, n_shared=shared, zipf=zipf)
+    inp = synth.make_inputs(wl, seed=7)
+    if zipf:
+        inp["router_b"] = inp["router_b"] * 8.0     # push hard: some experts get no rows
+    layer = h.make_layer(wl, inp)
+    r = h.route(layer, inp["x"])
+    layer.close()
+    counts = np.diff(r["expert_offsets"])
+    if zipf:
+        assert counts.min() == 0 and counts.max() > 64
+    check_layer(h, wl, inp, 1)
+
+
+def test_zero_tokens_is_a_noop(h):
+    import moe_expert_ffn_02_gb300 as moe
+    wl = synth.WORKLOADS["tiny"]
+    inp = synth.make_inputs(wl, seed=0)
+    layer = h.make_layer(wl, inp)
+    off = torch.full((wl.n_experts + 1,), 7, dtype=torch.int32, device="cuda")
+    ws, nb = layer.workspace(0, moe.MODE_PREFILL)
+    moe.moe_forward_prefill(layer.handle, 0, 0, 0, {"expert_offsets": off.data_ptr()}, ws, nb, layer.stream)
+    torch.cuda.synchronize()
+    assert not off.any()
+    with pytest.raises(moe.MoeError):
+        moe.moe_forward_decode(layer.handle, 0, 0, 0, None, ws, nb, layer.stream)
+    layer.close()
+
+
+def test_determinism_and_token_permutation(h):
+    wl = small_wl(16, 4, H=384, I=256, T=200)
+    inp = synth.make_inputs(wl, seed=9)
+    layer = h.make_layer(wl, inp)
+    y1, _ = h.run_forward(layer, inp["x"], 1, want_dbg=False)
+    y2, _ = h.run_forward(layer, inp["x"], 1, want_dbg=False)
+    assert np.array_equal(y1, y2)
+    perm = np.random.default_rng(3).permutation(wl.T)
+    yp, _ = h.run_forward(layer, inp["x"][perm], 1, want_dbg=False)
+    assert np.array_equal(yp, y1[perm])
+    # decode and prefill entries compute the same function
+    yd, _ = h.run_forward(layer, inp["x"][:64], 2, want_dbg=False)
+    yq, _ = h.run_forward(layer, inp["x"][:64], 1, want_dbg=False)
+    assert np.array_equal(yd, yq)
+    layer.close()
+
+
+def test_host_entry_matches_device_entry(h):
+    import moe_expert_ffn_02_gb300 as moe
+    wl = small_wl(16, 4, H=384, I=256, T=50)
+    inp = synth.make_inputs(wl, seed=11)
+    layer = h.make_layer(wl, inp)
+    y_dev, _ = h.run_forward(layer, inp["x"], 1, want_dbg=False)
+    xh = torch.from_numpy(inp["x"].view(np.int16)).pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    for mode in (1, 2):
+        ws, nb = layer.workspace(wl.T, mode)
+        moe.moe_forward_host(layer.handle, mode, xh.data_ptr(), wl.T, yh.data_ptr(), ws, nb, layer.stream)
+        assert np.array_equal(yh.numpy().view(np.uint16), y_dev)
+    layer.close()
+
+
+def test_bounded_wait_reports_timeout_without_fault(h):
+    import moe_expert_ffn_02_gb300 as moe
+    wl = synth.WORKLOADS["tiny"]
+    inp = synth.make_inputs(wl, seed=0)
+    layer = h.make_layer(wl, inp)
+    moe.moe_set_wait_limit(layer.handle, 2000)          # 2 ms
+    moe.moe_debug_timeout_probe(layer.handle, layer.stream)
+    st, flags = moe.moe_get_device_status(layer.handle, layer.stream)
+    assert st == 6 and flags & moe.DEV_WAIT_TIMEOUT      # MOE_ERR_TIMEOUT
+    st, flags = moe.moe_get_device_status(layer.handle, layer.stream)
+    assert st == 0 and flags == 0                        # read-and-clear
+    # the context is still usable
+    moe.moe_set_wait_limit(layer.handle, 2_000_000)
+    check_layer(h, wl, inp, 1)
+    layer.close()
+
+
+def test_argument_errors_enqueue_nothing(h):
+    import moe_expert_ffn_02_gb300 as moe
+    wl = synth.WORKLOADS["tiny"]
+    inp = synth.make_inputs(wl, seed=0)
+    layer = h.make_layer(wl, inp)
+    ws, nb = layer.workspace(8, moe.MODE_PREFILL)
+    x = torch.zeros((8, wl.hidden), dtype=torch.int16, device="cuda")
+    y = torch.zeros_like(x)
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_forward_prefill(layer.handle, x.data_ptr(), 8, y.data_ptr(), None, ws, 1024, layer.stream)
+    assert e.value.status == 3                           # MOE_ERR_WORKSPACE
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_forward_prefill(layer.handle, x.data_ptr() + 2, 8, y.data_ptr(), None, ws, nb, layer.stream)
+    assert e.value.status == 1
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_forward_decode(layer.handle, x.data_ptr(), 65, y.data_ptr(), None, ws, nb, layer.stream)
+    assert e.value.status == 2
+    assert not y.any()
+    layer.close()
+
+
+# ------------------------------------------------------------------ full-size configurations
+
+def sample_rows(T, r, n_rand=48, seed=0):
+    """Tokens to check one by one: both ends, random ones, and every token of
+    the most loaded expert (up to 64) so a full multi-tile group is covered."""
+    rng = np.random.default_rng(seed)
+    rows = set(range(min(8, T))) | set(range(max(0, T - 8), T))
+    rows |= set(rng.choice(T, size=min(n_rand, T), replace=False).tolist())
+    counts = np.diff(r["offsets"])
+    hot = int(np.argmax(counts))
+    hot_tokens = r["sorted_token"][r["offsets"][hot]:r["offsets"][hot + 1]]
+    rows |= set(hot_tokens[:32].tolist()) | set(hot_tokens[-32:].tolist())
+    return np.array(sorted(rows), dtype=np.int32)
+
+
+@pytest.mark.parametrize("name", ["ds_decode_t1", "ds_decode_t4", "ds_decode_t16"])
+def test_deepseek_decode_layer(h, ds_inputs, name):
+    wl = synth.WORKLOADS[name]
+    base = ds_inputs
+    inp = dict(base, x=synth.bf16_normal(0, synth.STREAM_X, (wl.T, wl.hidden)))
+    layer = h.make_layer(wl, inp)
+    y, dbg = h.run_forward(layer, inp["x"], 2)
+    r = h.route(layer, inp["x"])
+    Lref = oracle.logits(inp["x"], inp["router_w"], None)
+    assert np.all(np.abs(r["logits"] - Lref) <= 1e-5 * (1 + np.abs(Lref)))
+    ref_route = oracle.route_from_logits(r["logits"], wl.top_k)
+    h.assert_routing_equal(dbg, ref_route)
+    y_ref = oracle.forward(inp, wl.top_k, ref_route["ids"], ref_route["w"])
+    h.compare_y(y, y_ref)
+    layer.close()
+
+
+@pytest.fixture(scope="module")
+def ds_inputs():
+    wl = synth.WORKLOADS["ds_prefill_8k"]
+    return synth.make_inputs(wl, seed=0)
+
+
+@pytest.mark.parametrize("name", ["ds_prefill_8k", "skew_32k"])
+def test_deepseek_prefill_layers_sampled(h, ds_inputs, name):
+    wl = synth.WORKLOADS[name]
+    inp = dict(ds_inputs, x=synth.bf16_normal(0, synth.STREAM_X, (wl.T, wl.hidden)), router_b=synth.router_bias(wl, 0))
+    layer = h.make_layer(wl, inp)
+    y, dbg = h.run_forward(layer, inp["x"], 1)
+    r = h.route(layer, inp["x"])
+    ref_route = oracle.route_from_logits(r["logits"], wl.top_k)
+    h.assert_routing_equal(dbg, ref_route)
+    counts = np.diff(ref_route["offsets"])
+    if name == "skew_32k":
+        mean = wl.T * wl.top_k / wl.n_experts
+        assert counts.max() > 10 * mean and counts.min() == 0
+    rows = sample_rows(wl.T, ref_route)
+    sub = np.sort(rows)
+    Lref = oracle.logits(inp["x"][sub], inp["router_w"], inp["router_b"])
+    assert np.all(np.abs(r["logits"][sub] - Lref) <= 1e-5 * (1 + np.abs(Lref)))
+    y_ref = oracle.forward(inp, wl.top_k, ref_route["ids"], ref_route["w"], rows=sub)
+    h.compare_y(y[sub], y_ref)
+    layer.close()
+
+
+def test_kimi_prefill_layer_sampled(h):
+    wl = synth.WORKLOADS["kimi_64k"]
+    inp = synth.make_inputs(wl, seed=0)
+    layer = h.make_layer(wl, inp)
+    y, dbg = h.run_forward(layer, inp["x"], 1, want_dbg=True)
+    r = h.route(layer, inp["x"])
+    ref_route = oracle.route_from_logits(r["logits"], wl.top_k)
+    h.assert_routing_equal(dbg, ref_route)
+    rows = sample_rows(wl.T, ref_route, n_rand=32)
+    y_ref = oracle.forward(inp, wl.top_k, ref_route["ids"], ref_route["w"], rows=rows)
+    h.compare_y(y[rows], y_ref)
+    layer.close()
