@@ -52,7 +52,7 @@ L2_FLUSH_BYTES = 512 << 20
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--steps", type=int, default=None, help="timed steps (default 300 decode, 20 prefill)")
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--workload", default="ds_decode_t16", choices=sorted(synth.WORKLOADS))
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -61,6 +61,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     a = p.parse_args()
     a.warmup = max(a.warmup, 3)
+    if a.steps is None:
+        a.steps = 300 if synth.WORKLOADS[a.workload].T <= 64 else 20
     return a
 
 
@@ -101,7 +103,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()

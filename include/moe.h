@@ -128,6 +128,10 @@ typedef struct {
     int32_t* inv_row;            /* [T][k] row of (token, slot)                 */
     uint8_t* xq;                 /* [T][H] E4M3FN codes of x (forward only)     */
     float* sx;                   /* [T][H/128] multipliers of xq (forward only) */
+    uint8_t* hq;                 /* [T][k+n_shared][I] E4M3FN codes of h per    */
+                                 /*   (token, slot): routed slots in rank       */
+                                 /*   order, then the shared expert (forward)   */
+    float* sh;                   /* [T][k+n_shared][I/128] multipliers of hq    */
 } moe_route_out;
 
 /* Build a layer: validate desc, allocate the layer's device memory, repack

@@ -49,7 +49,7 @@ class MoeWeights(ctypes.Structure):
 
 class MoeRouteOut(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
-        "logits", "topk_ids", "topk_w", "expert_offsets", "sorted_token", "inv_row", "xq", "sx")]
+        "logits", "topk_ids", "topk_w", "expert_offsets", "sorted_token", "inv_row", "xq", "sx", "hq", "sh")]
 
 
 _lock = threading.Lock()

@@ -42,21 +42,32 @@ moe::WsLayout make_layout(const moe_layer* L, int T, int mode) {
     moe::WsLayout l{};
     const size_t E = L->d.n_experts, k = L->d.top_k, H = L->d.hidden, I = L->d.inter;
     const size_t R = (size_t)T * k;
-    const size_t rows = R + (L->d.n_shared ? (size_t)T : 0);
+    // internal rows: every routed group padded to ROW_ALIGN, then the shared group
+    const size_t rows = R + (L->d.n_shared ? (size_t)T : 0) + (size_t)moe::ROW_ALIGN * (E + 1);
     l.rows_pad = (int)up(rows + moe::ROW_PAD, 64);
-    l.ksplit = (T <= 256) ? (int)(H / moe::QB) : 1;
+    // router: T <= 64 -> one GEMV pass (ksplit 0); otherwise the tiled GEMM,
+    // split along H (a divisor of H/128) until the grid covers ~2 waves
+    if (T <= 64) {
+        l.ksplit = 0;
+    } else {
+        const int base = (int)((E + 63) / 64) * ((T + 63) / 64), hb = (int)(H / moe::QB);
+        l.ksplit = 1;
+        for (int d = 1; d <= hb; ++d)
+            if (hb % d == 0 && base * d <= 2 * L->num_sms) l.ksplit = d;
+    }
     l.n_chunks = (T + moe::CHUNK_TOK - 1) / moe::CHUNK_TOK;
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t o = off; off = up(off + bytes, 256); return o; };
-    l.logit_part = take((size_t)l.ksplit * T * E * 4);
+    l.logit_part = take((size_t)(l.ksplit > 0 ? l.ksplit : 1) * T * E * 4);
     l.logits = l.logit_part;
     l.ids = take(R * 4);
     l.w = take(R * 4);
     l.chunk_cnt = take((size_t)l.n_chunks * E * 4);
     l.chunk_base = take((size_t)l.n_chunks * E * 4);
     l.offsets = take((E + 1) * 4);
-    l.sorted_tok = 0;
+    l.offsets_pad = take((E + 1) * 4);
     l.inv_row = take(R * 4);
+    l.inv_int = take(R * 4);
     l.table = take(sizeof(moe::GroupTable));
     if (mode != MOE_MODE_ROUTE) {
         l.xp = take((size_t)l.rows_pad * H);
@@ -99,7 +110,7 @@ moe_status check_call(moe_layer* L, int T, int mode, const void* x, const void* 
 // Routing stage shared by every entry.  `logits_in` != NULL: route from
 // given logits (no router GEMM, no bias).
 moe_status run_route(moe_layer* L, const uint16_t* x, const float* logits_in, int T, const moe::WsLayout& lay,
-                     char* ws, const moe_route_out* dbg, cudaStream_t s) {
+                     char* ws, const moe_route_out* dbg, cudaStream_t s, int bn = kBN) {
     const int k = L->d.top_k;
     int32_t* ids = reinterpret_cast<int32_t*>(ws + lay.ids);
     float* w = reinterpret_cast<float*>(ws + lay.w);
@@ -108,7 +119,9 @@ moe_status run_route(moe_layer* L, const uint16_t* x, const float* logits_in, in
     } else {
         float* part = reinterpret_cast<float*>(ws + lay.logit_part);
         MOE_CUDA(moe::launch_router_logits(L, x, T, part, lay.ksplit, s), "router logits");
-        MOE_CUDA(moe::launch_topk(L, part, lay.ksplit, true, T, dbg ? dbg->logits : nullptr, ids, w, s), "top-k");
+        MOE_CUDA(moe::launch_topk(L, part, lay.ksplit > 0 ? lay.ksplit : 1, true, T, dbg ? dbg->logits : nullptr, ids,
+                                  w, s),
+                 "top-k");
     }
     if (dbg && dbg->topk_ids)
         MOE_CUDA(cudaMemcpyAsync(dbg->topk_ids, ids, sizeof(int32_t) * (size_t)T * k, cudaMemcpyDeviceToDevice, s),
@@ -116,7 +129,7 @@ moe_status run_route(moe_layer* L, const uint16_t* x, const float* logits_in, in
     if (dbg && dbg->topk_w)
         MOE_CUDA(cudaMemcpyAsync(dbg->topk_w, w, sizeof(float) * (size_t)T * k, cudaMemcpyDeviceToDevice, s),
                  "copy weights");
-    MOE_CUDA(moe::launch_permute(L, ids, T, lay, ws, kBN, dbg ? dbg->expert_offsets : nullptr,
+    MOE_CUDA(moe::launch_permute(L, ids, T, lay, ws, bn, dbg ? dbg->expert_offsets : nullptr,
                                  dbg ? dbg->sorted_token : nullptr, dbg ? dbg->inv_row : nullptr, s),
              "permutation");
     return MOE_OK;
@@ -139,13 +152,15 @@ moe_status run_forward(moe_layer* L, int mode, const uint16_t* x, int T, uint16_
         return cudaEventRecord(L->ev[i], s);
     };
     MOE_CUDA(mark(0), "profile event");
-    st = run_route(L, x, nullptr, T, lay, ws, dbg, s);
+    st = run_route(L, x, nullptr, T, lay, ws, dbg, s, kBN);
     if (st != MOE_OK) return st;
     MOE_CUDA(mark(1), "profile event");
     MOE_CUDA(moe::launch_quant_scatter(L, x, T, lay, ws, dbg ? dbg->xq : nullptr, dbg ? dbg->sx : nullptr, s),
              "activation quantisation");
     MOE_CUDA(mark(2), "profile event");
     MOE_CUDA(moe::launch_expert_gate_up(L, T, lay, ws, kBN, 0, s), "gate/up GEMM");
+    if (dbg && (dbg->hq || dbg->sh))
+        MOE_CUDA(moe::launch_h_gather(L, T, lay, ws, dbg->hq, dbg->sh, s), "h debug copy");
     MOE_CUDA(mark(3), "profile event");
     MOE_CUDA(moe::launch_expert_down(L, T, lay, ws, kBN, 0, s), "down GEMM");
     MOE_CUDA(mark(4), "profile event");

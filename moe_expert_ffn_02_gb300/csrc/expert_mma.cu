@@ -34,7 +34,7 @@ namespace moe {
 constexpr int BN = 64;                  // rows (tokens) per n tile
 constexpr int CW = 8;                   // consumer warps (16 output rows each)
 constexpr int NTHREADS = (CW + 1) * 32; // + producer warp
-constexpr int XSTRIDE = 144;            // padded activation row in shared memory
+constexpr int XSTRIDE = 128;            // activation row in shared memory (swizzled)
 
 template <bool GU>
 struct Cfg {
@@ -49,12 +49,12 @@ struct Cfg {
 struct ExpertArgs {
     const uint8_t* w;         // tile images of all groups
     const float* wscale;      // per (group, m tile, k tile) [x2 for gate/up]
-    const uint8_t* act;       // activation rows [rows_pad][K] (E4M3)
+    const uint8_t* act;       // activations [K/128][rows_pad][128] (E4M3, swizzled)
     const float* actsT;       // activation scales [K/128][ld]
-    int ld;                   // row stride of actsT / shT (rows_pad)
+    int ld;                   // rows_pad of the permuted buffers
     int K, M;                 // reduction length, output features
     const GroupTable* gt;
-    uint8_t* hq;              // gate/up: [rows][M] E4M3 h
+    uint8_t* hq;              // gate/up: [M/128][rows_pad][128] E4M3 h (swizzled)
     float* shT;               // gate/up: [M/128][ld]
     float* out;               // down: [rows][M] fp32
     uint32_t* status;
@@ -125,11 +125,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_gemm_kernel(ExpertArgs a) 
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&full[stage], C::W_BYTES + un.valid * QB);
                     bulk_g2s(st, wbase + (size_t)kb * C::W_BYTES, C::W_BYTES, &full[stage]);
+                    bulk_g2s(st + C::W_BYTES, a.act + act_offset(kb, un.row_begin, a.ld), un.valid * QB,
+                             &full[stage]);
                 }
                 __syncwarp();
-                for (int r = lane; r < un.valid; r += 32)
-                    bulk_g2s(st + C::W_BYTES + r * XSTRIDE, a.act + (size_t)(un.row_begin + r) * a.K + kb * QB, QB,
-                             &full[stage]);
                 armed |= 1u << stage;
                 armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
                 if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
@@ -196,8 +195,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_gemm_kernel(ExpertArgs a) 
 #pragma unroll
             for (int nt = 0; nt < BN / 8; ++nt) {
                 if (nt < nt_active) {
-                    const uint8_t* xr = X + (nt * 8 + g) * XSTRIDE;
-                    const uint4 xb0 = lds128(xr + (2 * q) * 16), xb1 = lds128(xr + (2 * q + 1) * 16);
+                    const uint8_t* xr = X + (nt * 8 + g) * XSTRIDE;      // row & 7 == g: same swizzle as A
+                    const uint4 xb0 = lds128(xr + c0), xb1 = lds128(xr + c1);
                     const uint32_t Bx[8] = {xb0.x, xb0.y, xb0.z, xb0.w, xb1.x, xb1.y, xb1.z, xb1.w};
                     float pg[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -230,7 +229,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_gemm_kernel(ExpertArgs a) 
 
         if (GU) {
             // ---------------------------------------------- SiLU(g)*u, 1x128 quantisation
-            uint8_t* qst = epi;                                   // [BN][144] codes
+            uint8_t* qst = epi;                                   // [BN][144] codes (unswizzled)
             float* amax_s = reinterpret_cast<float*>(epi + BN * 144);   // [CW][BN]
             float h[BN / 8][4];
 #pragma unroll
@@ -270,11 +269,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_gemm_kernel(ExpertArgs a) 
                 }
             }
             named_bar_sync(1, CW * 32);
-            // 16 bytes per thread, 8 rows per pass
+            // 16 bytes per thread, 8 rows per pass, into the swizzled K-block-major layout
             const int tid = threadIdx.x;
             for (int rr = tid >> 3; rr < un.valid; rr += (CW * 32) >> 3) {
                 const uint4 v = lds128(qst + rr * 144 + (tid & 7) * 16);
-                *reinterpret_cast<uint4*>(a.hq + (size_t)(un.row_begin + rr) * a.M + un.mb * QB + (tid & 7) * 16) = v;
+                const int pos = (tid & 7) ^ (rr & 7);                 // row_begin is a multiple of 8
+                *reinterpret_cast<uint4*>(a.hq + act_offset(un.mb, un.row_begin + rr, a.ld) + pos * 16) = v;
             }
             named_bar_sync(1, CW * 32);
         } else {
@@ -358,19 +358,19 @@ cudaError_t launch_expert_down(const moe_layer* L, int T, const WsLayout& lay, c
 // in fp32, rounded once to bf16.  One CTA per token, 4 channels per thread
 // per step.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ O, const int32_t* __restrict__ inv_row,
-                                                      const float* __restrict__ w, const int32_t* __restrict__ offsets,
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ O, const int32_t* __restrict__ inv_int,
+                                                      const float* __restrict__ w, const int32_t* __restrict__ offsets_pad,
                                                       int T, int H, int k, int E, int n_shared,
                                                       uint16_t* __restrict__ y) {
     __shared__ int rows[MAX_TOPK];
     __shared__ float wt[MAX_TOPK];
     const int t = blockIdx.x;
     if (threadIdx.x < k) {
-        rows[threadIdx.x] = inv_row[(size_t)t * k + threadIdx.x];
+        rows[threadIdx.x] = inv_int[(size_t)t * k + threadIdx.x];
         wt[threadIdx.x] = w[(size_t)t * k + threadIdx.x];
     }
     __syncthreads();
-    const size_t shrow = (size_t)offsets[E] + t;
+    const size_t shrow = (size_t)offsets_pad[E] + t;
     for (int c = threadIdx.x * 4; c < H; c += blockDim.x * 4) {
         float4 acc = n_shared ? *reinterpret_cast<const float4*>(O + shrow * H + c) : make_float4(0.f, 0.f, 0.f, 0.f);
         for (int j = 0; j < k; ++j) {
@@ -393,10 +393,47 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 cudaError_t launch_combine(const moe_layer* L, int T, const WsLayout& lay, char* ws, uint16_t* y, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     combine_kernel<<<T, 256, 0, s>>>(reinterpret_cast<const float*>(ws + lay.o),
-                                     reinterpret_cast<const int32_t*>(ws + lay.inv_row),
+                                     reinterpret_cast<const int32_t*>(ws + lay.inv_int),
                                      reinterpret_cast<const float*>(ws + lay.w),
-                                     reinterpret_cast<const int32_t*>(ws + lay.offsets), T, L->d.hidden, L->d.top_k,
+                                     reinterpret_cast<const int32_t*>(ws + lay.offsets_pad), T, L->d.hidden, L->d.top_k,
                                      L->d.n_experts, L->d.n_shared, y);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Debug copy of the h codes and scales per (token, slot), slots 0..k-1 the
+// routed experts in rank order and slot k the shared expert, unswizzled:
+// hq_out [T][S][I], sh_out [T][S][I/128].  One CTA per token.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) h_gather_kernel(const uint8_t* __restrict__ hq, const float* __restrict__ shT,
+                                                       int ld, const int32_t* __restrict__ inv_int,
+                                                       const int32_t* __restrict__ offsets_pad, int E, int k, int S,
+                                                       int I, uint8_t* __restrict__ hq_out, float* __restrict__ sh_out) {
+    const int t = blockIdx.x;
+    const int IB = I / QB;
+    for (int slot = 0; slot < S; ++slot) {
+        const int row = slot < k ? inv_int[(size_t)t * k + slot] : offsets_pad[E] + t;
+        const size_t rec = (size_t)t * S + slot;
+        if (hq_out)
+            for (int c = threadIdx.x; c < IB * 8; c += blockDim.x) {
+                const int ib = c >> 3, ch = c & 7;
+                const uint4 v = *reinterpret_cast<const uint4*>(hq + act_offset(ib, row, ld) + ((ch ^ (row & 7)) * 16));
+                *reinterpret_cast<uint4*>(hq_out + rec * I + ib * QB + ch * 16) = v;
+            }
+        if (sh_out)
+            for (int ib = threadIdx.x; ib < IB; ib += blockDim.x) sh_out[rec * IB + ib] = shT[(size_t)ib * ld + row];
+    }
+}
+
+cudaError_t launch_h_gather(const moe_layer* L, int T, const WsLayout& lay, char* ws, uint8_t* hq_out, float* sh_out,
+                            cudaStream_t s) {
+    if (T == 0 || (!hq_out && !sh_out)) return cudaSuccess;
+    const int S = L->d.top_k + L->d.n_shared;
+    h_gather_kernel<<<T, 128, 0, s>>>(reinterpret_cast<const uint8_t*>(ws + lay.hq),
+                                      reinterpret_cast<const float*>(ws + lay.shT), lay.rows_pad,
+                                      reinterpret_cast<const int32_t*>(ws + lay.inv_int),
+                                      reinterpret_cast<const int32_t*>(ws + lay.offsets_pad), L->d.n_experts,
+                                      L->d.top_k, S, L->d.inter, hq_out, sh_out);
     return cudaGetLastError();
 }
 

@@ -14,7 +14,21 @@ constexpr int QB = 128;               // quantisation / scale block edge
 constexpr int TILE_BYTES = QB * QB;   // one 128x128 FP8 weight tile image
 constexpr int MAX_TOPK = 32;
 constexpr int MAX_EXPERTS = 1024;
-constexpr int ROW_PAD = 128;          // spare rows after every permuted buffer
+constexpr int ROW_PAD = 256;          // spare rows after every permuted buffer
+constexpr int ROW_ALIGN = 8;          // each group's rows start on a multiple of 8
+
+// ---------------------------------------------------------------------------
+// Permuted activation buffers (x codes, h codes) use the same 128-byte
+// swizzle as the weight tiles, stored K-block-major:
+//   buf[kb][row][128 B], 16-byte chunk c of (kb, row) at chunk c ^ (row & 7).
+// Every group starts on a multiple of 8 rows, so the rows [r, r + n) of one
+// K block are one contiguous, already-swizzled n x 128 B image: a single
+// bulk copy moves an operand tile for either GEMM.  Their scales are
+// K-block-major too: s[kb][row].
+// ---------------------------------------------------------------------------
+__host__ __device__ inline size_t act_offset(int kb, int row, int rows_pad) {
+    return ((size_t)kb * rows_pad + row) * 128;
+}
 
 // ---------------------------------------------------------------------------
 // Weight tile image.  A [R][C] FP8 matrix (C contiguous) is stored as tiles
@@ -36,9 +50,9 @@ struct GroupTable {
     int32_t n_groups;
     int32_t n_pairs;        // sum over groups of ceil(rows / bn)
     int32_t bn;             // n-tile height used to build the table
-    int32_t total_rows;     // R + T (rows of the permuted buffers)
+    int32_t total_rows;     // internal rows in use (padded groups + shared)
     int32_t expert[MAX_EXPERTS + 1];
-    int32_t row0[MAX_EXPERTS + 1];
+    int32_t row0[MAX_EXPERTS + 1];   // internal (8-aligned) first row
     int32_t rows[MAX_EXPERTS + 1];
     int32_t pair_start[MAX_EXPERTS + 2];
 };
@@ -51,15 +65,16 @@ struct WsLayout {
     size_t w;            // f32 [T][k]
     size_t chunk_cnt;    // i32 [n_chunks][E]
     size_t chunk_base;   // i32 [n_chunks][E]
-    size_t offsets;      // i32 [E+1]
-    size_t sorted_tok;   // i32 [T*k]
-    size_t inv_row;      // i32 [T][k]
+    size_t offsets;      // i32 [E+1]   canonical expert offsets
+    size_t offsets_pad;  // i32 [E+1]   internal 8-aligned group starts (E: shared)
+    size_t inv_row;      // i32 [T][k]  canonical row of (token, slot)
+    size_t inv_int;      // i32 [T][k]  internal row of (token, slot)
     size_t table;        // GroupTable
-    size_t xp;           // u8  [rows+pad][H]   permuted quantised x
-    size_t sxT;          // f32 [H/128][rows+pad]
-    size_t hq;           // u8  [rows+pad][I]   quantised h
-    size_t shT;          // f32 [I/128][rows+pad]
-    size_t o;            // f32 [rows][H]       expert outputs (unweighted)
+    size_t xp;           // u8  [H/128][rows_pad][128]  permuted quantised x (swizzled)
+    size_t sxT;          // f32 [H/128][rows_pad]
+    size_t hq;           // u8  [I/128][rows_pad][128]  quantised h (swizzled)
+    size_t shT;          // f32 [I/128][rows_pad]
+    size_t o;            // f32 [rows_pad][H]           expert outputs (unweighted)
     size_t total;
     int ksplit, n_chunks, rows_pad;
 };
@@ -212,6 +227,8 @@ cudaError_t launch_expert_gate_up(const moe_layer* L, int T, const WsLayout& lay
                                   cudaStream_t s);
 cudaError_t launch_expert_down(const moe_layer* L, int T, const WsLayout& lay, char* ws, int bn, int max_units,
                                cudaStream_t s);
+cudaError_t launch_h_gather(const moe_layer* L, int T, const WsLayout& lay, char* ws, uint8_t* hq_out, float* sh_out,
+                            cudaStream_t s);
 cudaError_t launch_combine(const moe_layer* L, int T, const WsLayout& lay, char* ws, uint16_t* y, cudaStream_t s);
 cudaError_t launch_timeout_probe(const moe_layer* L, cudaStream_t s);
 }  // namespace moe

@@ -113,10 +113,80 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __re
     }
 }
 
+// ---------------------------------------------------------------------------
+// Router logits for a decode batch (T <= 64): a GEMV over the fp32 router
+// weights, which dominate the bytes.  One CTA per pair of experts; warp w
+// owns channels [w*H/8, (w+1)*H/8); each lane accumulates its channels in
+// fp32 for every token, the lanes are combined by a shuffle tree and the
+// warps in a fixed order -- deterministic, and no partial sums leave the CTA.
+// ---------------------------------------------------------------------------
+constexpr int GEMV_E = 2, GEMV_WARPS = 8, GEMV_TMAX = 64;
+
+__global__ void __launch_bounds__(GEMV_WARPS * 32) router_gemv_kernel(const uint16_t* __restrict__ x,
+                                                                      const float* __restrict__ W, int T, int H,
+                                                                      int E, float* __restrict__ logits) {
+    __shared__ float red[GEMV_WARPS][GEMV_E][GEMV_TMAX];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e0 = blockIdx.x * GEMV_E;
+    const int span = H / GEMV_WARPS;                   // multiple of 16
+    const int h0 = warp * span;
+    for (int t0 = 0; t0 < T; t0 += 8) {                // 8 tokens at a time keeps the accumulators in registers
+        float acc[GEMV_E][8];
+#pragma unroll
+        for (int j = 0; j < GEMV_E; ++j)
+#pragma unroll
+            for (int u = 0; u < 8; ++u) acc[j][u] = 0.f;
+        for (int h = h0 + lane * 4; h < h0 + span; h += 128) {
+            float4 wv[GEMV_E];
+#pragma unroll
+            for (int j = 0; j < GEMV_E; ++j)
+                wv[j] = (e0 + j < E) ? *reinterpret_cast<const float4*>(W + (size_t)(e0 + j) * H + h)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (t0 + u < T) {
+                    const uint2 raw = *reinterpret_cast<const uint2*>(x + (size_t)(t0 + u) * H + h);
+                    const float a0 = __uint_as_float(raw.x << 16), a1 = __uint_as_float(raw.x & 0xFFFF0000u);
+                    const float a2 = __uint_as_float(raw.y << 16), a3 = __uint_as_float(raw.y & 0xFFFF0000u);
+#pragma unroll
+                    for (int j = 0; j < GEMV_E; ++j) {
+                        float p = __fmul_rn(a0, wv[j].x);
+                        p = __fmaf_rn(a1, wv[j].y, p);
+                        p = __fmaf_rn(a2, wv[j].z, p);
+                        p = __fmaf_rn(a3, wv[j].w, p);
+                        acc[j][u] = __fadd_rn(acc[j][u], p);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < GEMV_E; ++j)
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                float v = acc[j][u];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
+                if (lane == 0 && t0 + u < T) red[warp][j][t0 + u] = v;
+            }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < GEMV_E * T; i += blockDim.x) {
+        const int j = i / T, t = i - j * T;
+        if (e0 + j >= E) continue;
+        float v = red[0][j][t];
+        for (int w = 1; w < GEMV_WARPS; ++w) v = __fadd_rn(v, red[w][j][t]);
+        logits[(size_t)t * E + e0 + j] = v;
+    }
+}
+
 cudaError_t launch_router_logits(const moe_layer* L, const uint16_t* x, int T, float* part, int ksplit,
                                  cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     const int H = L->d.hidden, E = L->d.n_experts;
+    if (ksplit == 0) {                                 // decode batch: GEMV, complete logits in part[0]
+        router_gemv_kernel<<<(E + GEMV_E - 1) / GEMV_E, GEMV_WARPS * 32, 0, s>>>(x, L->router_w, T, H, E, part);
+        return cudaGetLastError();
+    }
     dim3 grid((E + LE - 1) / LE, (T + LT - 1) / LT, ksplit);
     router_logits_kernel<<<grid, 256, 0, s>>>(x, L->router_w, T, H, E, H / ksplit, part);
     return cudaGetLastError();
@@ -320,6 +390,7 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(const int32_t* __restri
                                                          int E, int k, int n_shared, int bn,
                                                          int32_t* __restrict__ chunk_base,
                                                          int32_t* __restrict__ offsets,
+                                                         int32_t* __restrict__ offsets_pad,
                                                          int32_t* __restrict__ offsets_out, GroupTable* gt) {
     __shared__ int total_s;
     const int e = threadIdx.x;
@@ -333,13 +404,19 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(const int32_t* __restri
     }
     const int off = block_excl_scan_1024(e < E ? tot : 0, &total_s);
     const int R = total_s;
+    // internal row space: every group starts on a multiple of ROW_ALIGN rows
+    const int padded = (e < E) ? (tot + ROW_ALIGN - 1) / ROW_ALIGN * ROW_ALIGN : 0;
+    const int poff = block_excl_scan_1024(padded, &total_s);
+    const int shared_row0 = total_s;
     if (e < E) {
         offsets[e] = off;
+        offsets_pad[e] = poff;
         if (offsets_out) offsets_out[e] = off;
         for (int c = 0; c < n_chunks; ++c) chunk_base[(size_t)c * E + e] += off;
     }
     if (e == 0) {
         offsets[E] = R;
+        offsets_pad[E] = shared_row0;
         if (offsets_out) offsets_out[E] = R;
     }
     // group table: active experts in index order, then the shared expert
@@ -351,7 +428,7 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(const int32_t* __restri
     const int routed_pairs = total_s;
     if (active) {
         gt->expert[gidx] = e;
-        gt->row0[gidx] = off;
+        gt->row0[gidx] = poff;
         gt->rows[gidx] = tot;
         gt->pair_start[gidx] = pstart;
     }
@@ -359,7 +436,7 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(const int32_t* __restri
         int ng = n_routed, np = routed_pairs;
         if (n_shared && T > 0) {
             gt->expert[ng] = E;
-            gt->row0[ng] = R;
+            gt->row0[ng] = shared_row0;
             gt->rows[ng] = T;
             gt->pair_start[ng] = np;
             np += (T + bn - 1) / bn;
@@ -369,14 +446,17 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(const int32_t* __restri
         gt->n_groups = ng;
         gt->n_pairs = np;
         gt->bn = bn;
-        gt->total_rows = R + (n_shared ? T : 0);
+        gt->total_rows = shared_row0 + (n_shared ? T : 0);
     }
 }
 
 __global__ void __launch_bounds__(128) perm_scatter_kernel(const int32_t* __restrict__ ids, int T, int E, int k,
                                                            int n_chunks, const int32_t* __restrict__ chunk_base,
+                                                           const int32_t* __restrict__ offsets,
+                                                           const int32_t* __restrict__ offsets_pad,
                                                            int32_t* __restrict__ sorted_token,
-                                                           int32_t* __restrict__ inv_row, uint32_t* status) {
+                                                           int32_t* __restrict__ inv_row,
+                                                           int32_t* __restrict__ inv_int, uint32_t* status) {
     extern __shared__ int32_t run_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x * 4 + warp;
@@ -399,6 +479,7 @@ __global__ void __launch_bounds__(128) perm_scatter_kernel(const int32_t* __rest
             const int t = t0 + i / k;
             if (sorted_token) sorted_token[row] = t;
             inv_row[(size_t)t0 * k + i] = row;
+            inv_int[(size_t)t0 * k + i] = row - offsets[e] + offsets_pad[e];
         }
         __syncwarp();
         if (valid && (peers & lt_mask) == 0) run[e] += __popc(peers);
@@ -412,8 +493,10 @@ cudaError_t launch_permute(const moe_layer* L, const int32_t* ids, int T, const 
     int32_t* chunk_cnt = reinterpret_cast<int32_t*>(ws + lay.chunk_cnt);
     int32_t* chunk_base = reinterpret_cast<int32_t*>(ws + lay.chunk_base);
     int32_t* offsets = reinterpret_cast<int32_t*>(ws + lay.offsets);
+    int32_t* offsets_pad = reinterpret_cast<int32_t*>(ws + lay.offsets_pad);
     int32_t* sorted_token = sorted_out;   // only the caller needs it
     int32_t* inv_row = reinterpret_cast<int32_t*>(ws + lay.inv_row);
+    int32_t* inv_int = reinterpret_cast<int32_t*>(ws + lay.inv_int);
     GroupTable* gt = reinterpret_cast<GroupTable*>(ws + lay.table);
     const int nc = lay.n_chunks;
     const size_t smem = 4 * E * sizeof(int32_t);
@@ -422,13 +505,13 @@ cudaError_t launch_permute(const moe_layer* L, const int32_t* ids, int T, const 
         cudaError_t err = cudaGetLastError();
         if (err != cudaSuccess) return err;
     }
-    perm_scan_kernel<<<1, 1024, 0, s>>>(chunk_cnt, nc, T, E, k, L->d.n_shared, bn, chunk_base, offsets, offsets_out,
-                                        gt);
+    perm_scan_kernel<<<1, 1024, 0, s>>>(chunk_cnt, nc, T, E, k, L->d.n_shared, bn, chunk_base, offsets, offsets_pad,
+                                        offsets_out, gt);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     if (nc > 0) {
-        perm_scatter_kernel<<<(nc + 3) / 4, 128, smem, s>>>(ids, T, E, k, nc, chunk_base, sorted_token, inv_row,
-                                                            L->dev_status);
+        perm_scatter_kernel<<<(nc + 3) / 4, 128, smem, s>>>(ids, T, E, k, nc, chunk_base, offsets, offsets_pad,
+                                                            sorted_token, inv_row, inv_int, L->dev_status);
         err = cudaGetLastError();
         if (err != cudaSuccess) return err;
         if (inv_out)
@@ -441,14 +524,15 @@ cudaError_t launch_permute(const moe_layer* L, const int32_t* ids, int T, const 
 // 1x128 quantisation of x, written to every row the token owns.
 // Per token t and 128-channel group g: amax = max |x|; s = amax / 448
 // (s = 1 if amax = 0); q = E4M3FN(fp32(x / s)) rounded to nearest even with
-// saturation.  Destination rows: inv_row[t][0..k-1] (routed groups) and
-// R + t (shared group).  Scales are stored transposed, sxT[g][row], so a
-// tile of rows reads a contiguous run.  One CTA per token, one warp per
-// group at a time, 4 channels per lane.
+// saturation.  Destination rows (internal, 8-aligned groups): inv_int[t][j]
+// for the routed groups and shared_row0 + t for the shared group; the codes
+// go to the swizzled K-block-major layout (see act_offset) and the scales
+// to sxT[g][row], so one tile of rows is one contiguous run of both.  One
+// CTA per token, one warp per group at a time, 4 channels per lane.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __restrict__ x, int T, int H, int k,
-                                                            int n_shared, const int32_t* __restrict__ inv_row,
-                                                            const int32_t* __restrict__ offsets, int E,
+                                                            int n_shared, const int32_t* __restrict__ inv_int,
+                                                            const int32_t* __restrict__ offsets_pad, int E,
                                                             uint8_t* __restrict__ xp, float* __restrict__ sxT,
                                                             int ld, uint8_t* __restrict__ xq_out,
                                                             float* __restrict__ sx_out) {
@@ -456,8 +540,8 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __re
     const int t = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nd = k + (n_shared ? 1 : 0);
-    if (threadIdx.x < k) dest[threadIdx.x] = inv_row[(size_t)t * k + threadIdx.x];
-    if (threadIdx.x == 0 && n_shared) dest[k] = offsets[E] + t;
+    if (threadIdx.x < k) dest[threadIdx.x] = inv_int[(size_t)t * k + threadIdx.x];
+    if (threadIdx.x == 0 && n_shared) dest[k] = offsets_pad[E] + t;
     __syncthreads();
     const int G = H / QB;
     for (int g = warp; g < G; g += 8) {
@@ -471,7 +555,8 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __re
         const uint32_t q = pack4_e4m3(__fdiv_rn(v0, sc), __fdiv_rn(v1, sc), __fdiv_rn(v2, sc), __fdiv_rn(v3, sc));
         for (int d = 0; d < nd; ++d) {
             const int row = dest[d];
-            *reinterpret_cast<uint32_t*>(xp + (size_t)row * H + g * QB + lane * 4) = q;
+            const int chunk = (lane >> 2) ^ (row & 7);
+            *reinterpret_cast<uint32_t*>(xp + act_offset(g, row, ld) + chunk * 16 + (lane & 3) * 4) = q;
             if (lane == 0) sxT[(size_t)g * ld + row] = sc;
         }
         if (xq_out) *reinterpret_cast<uint32_t*>(xq_out + (size_t)t * H + g * QB + lane * 4) = q;
@@ -483,8 +568,8 @@ cudaError_t launch_quant_scatter(const moe_layer* L, const uint16_t* x, int T, c
                                  uint8_t* xq_out, float* sx_out, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     quant_scatter_kernel<<<T, 256, 0, s>>>(x, T, L->d.hidden, L->d.top_k, L->d.n_shared,
-                                           reinterpret_cast<const int32_t*>(ws + lay.inv_row),
-                                           reinterpret_cast<const int32_t*>(ws + lay.offsets), L->d.n_experts,
+                                           reinterpret_cast<const int32_t*>(ws + lay.inv_int),
+                                           reinterpret_cast<const int32_t*>(ws + lay.offsets_pad), L->d.n_experts,
                                            reinterpret_cast<uint8_t*>(ws + lay.xp),
                                            reinterpret_cast<float*>(ws + lay.sxT), lay.rows_pad, xq_out, sx_out);
     return cudaGetLastError();

@@ -59,6 +59,9 @@ def _lib():
             lib.oracle_route_from_logits.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp]
             lib.oracle_forward.argtypes = [ctypes.POINTER(_Layer), vp, i32, vp, vp, vp, i32, i32, i32, vp, vp]
             lib.oracle_forward.restype = ctypes.c_int
+            lib.oracle_forward_ex.argtypes = [ctypes.POINTER(_Layer), vp, i32, vp, vp, vp, i32, i32, vp, vp, vp, vp, vp,
+                                              i32, vp, vp]
+            lib.oracle_forward_ex.restype = ctypes.c_int
             lib.oracle_threads.restype = ctypes.c_int
             lib.oracle_e4m3_encode_n.argtypes = [vp, i64, vp]
             lib.oracle_e4m3_decode_n.argtypes = [vp, i64, vp]
@@ -138,9 +141,13 @@ def route_from_logits(L, k: int) -> dict:
 
 
 def forward(inp: dict, k: int, ids, w, rows=None, exact_act: bool = False, n_threads: int = 0,
-            want_f64: bool = False):
+            want_f64: bool = False, hq_in=None, sh_in=None, want_h: bool = False):
     """The layer on the host.  inp holds the arrays of synth.make_inputs.
-    Returns y as bf16 bits [n_rows][H] (and the fp64 sums when want_f64)."""
+    Returns y as bf16 bits [n_rows][H]; with want_f64 also the fp64 sums; with
+    want_h also a dict of this oracle's h records (h32, hq, sh), each
+    [n_rows][slots][I (/128)] with slots = k routed (rank order) + shared.
+    hq_in/sh_in ([T][slots][I], [T][slots][I/128]) override the h codes the
+    down projection consumes."""
     x = np.ascontiguousarray(inp["x"], dtype=np.uint16)
     T, H = x.shape
     wg = inp["w_gate"]
@@ -165,10 +172,25 @@ def forward(inp: dict, k: int, ids, w, rows=None, exact_act: bool = False, n_thr
     w = np.ascontiguousarray(w, dtype=np.float32)
     rws = None if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
     n = T if rws is None else rws.size
+    S = k + (1 if has_sh else 0)
+    Imax = max(I, SI)
     y = np.empty((n, H), dtype=np.uint16)
     y64 = np.empty((n, H), dtype=np.float64) if want_f64 else None
-    rc = _lib().oracle_forward(ctypes.byref(lay), x.ctypes.data, T, ids.ctypes.data, w.ctypes.data,
-                               _ptr(rws), n, 1 if exact_act else 0, n_threads, y.ctypes.data, _ptr(y64))
+    hrec = None
+    if want_h:
+        hrec = {"h32": np.empty((n, S, Imax), np.float32), "hq": np.empty((n, S, Imax), np.uint8),
+                "sh": np.empty((n, S, Imax // 128), np.float32)}
+    hq_in = None if hq_in is None else np.ascontiguousarray(hq_in, dtype=np.uint8).reshape(T, S, Imax)
+    sh_in = None if sh_in is None else np.ascontiguousarray(sh_in, dtype=np.float32).reshape(T, S, Imax // 128)
+    rc = _lib().oracle_forward_ex(ctypes.byref(lay), x.ctypes.data, T, ids.ctypes.data, w.ctypes.data,
+                                  _ptr(rws), n, 1 if exact_act else 0, _ptr(hq_in), _ptr(sh_in),
+                                  _ptr(hrec["h32"]) if hrec else None, _ptr(hrec["hq"]) if hrec else None,
+                                  _ptr(hrec["sh"]) if hrec else None, n_threads, y.ctypes.data, _ptr(y64))
     if rc != 0:
         raise ValueError("oracle_forward rejected its arguments")
-    return (y, y64) if want_f64 else y
+    out = [y]
+    if want_f64:
+        out.append(y64)
+    if want_h:
+        out.append(hrec)
+    return out[0] if len(out) == 1 else tuple(out)

@@ -255,6 +255,7 @@ static int g_dec_ready = 0;
 
 static void expert_ffn(const expert_view* ev, int exact_act,
                        const uint8_t* xq, const float* sx, const double* xe,
+                       const uint8_t* hq_in, const float* sh_in,
                        double* o, double* hbuf, float* h32, uint8_t* hq, float* sh) {
     const int32_t H = ev->H, I = ev->I, HB = H / QBLOCK, IB = I / QBLOCK;
     for (int32_t i = 0; i < I; ++i) {
@@ -285,6 +286,9 @@ static void expert_ffn(const expert_view* ev, int exact_act,
         h32[i] = (float)hv;
     }
     if (!exact_act) oracle_quant_1x128(h32, I, hq, sh);
+    /* down projection input: the codes just computed, or the caller's */
+    const uint8_t* hq_use = hq_in ? hq_in : hq;
+    const float* sh_use = hq_in ? sh_in : sh;
     for (int32_t j = 0; j < H; ++j) {
         const uint8_t* rd = ev->wd + (int64_t)j * I;
         double acc = 0.0;
@@ -294,8 +298,8 @@ static void expert_ffn(const expert_view* ev, int exact_act,
                 for (int32_t i = kb * QBLOCK; i < (kb + 1) * QBLOCK; ++i) p += g_dec[rd[i]] * hbuf[i];
                 acc += p * (double)ev->sd[(int64_t)(j / QBLOCK) * IB + kb];
             } else {
-                for (int32_t i = kb * QBLOCK; i < (kb + 1) * QBLOCK; ++i) p += g_dec[rd[i]] * g_dec[hq[i]];
-                acc += p * ((double)ev->sd[(int64_t)(j / QBLOCK) * IB + kb] * (double)sh[kb]);
+                for (int32_t i = kb * QBLOCK; i < (kb + 1) * QBLOCK; ++i) p += g_dec[rd[i]] * g_dec[hq_use[i]];
+                acc += p * ((double)ev->sd[(int64_t)(j / QBLOCK) * IB + kb] * (double)sh_use[kb]);
             }
         }
         o[j] = acc;
@@ -311,12 +315,24 @@ static void expert_ffn(const expert_view* ev, int exact_act,
  * Routing (ids, w) is an input so the layer can be evaluated under any
  * routing (normally oracle_route_from_logits on some fp32 logits).
  * rows: the tokens to evaluate (NULL = all T); outputs are [n_rows][H].
+ *
+ * h records, per (token, slot) with slots 0..k-1 the routed experts in rank
+ * order and slot k the shared expert, each Imax = max(I, SI) wide:
+ *   h32_out/hq_out/sh_out [n_rows][slots][Imax (/128)]  -- the fp32 h, its
+ *     E4M3 codes and 1x128 scales as this oracle computes them (optional);
+ *   hq_in/sh_in [T][slots][Imax (/128)] -- optional override: the down
+ *     projection then consumes these codes instead of its own.  Used to
+ *     evaluate the layer under another implementation's h codes where the
+ *     fp32 rounding of h sits on an E4M3 rounding boundary and either code
+ *     is a correct result (the same idea as routing under given logits).
  * Returns 0, or -1 on a bad argument.
  * ---------------------------------------------------------------------- */
-ORACLE_API int oracle_forward(const oracle_layer* L, const uint16_t* x, int32_t T,
-                              const int32_t* ids, const float* w,
-                              const int32_t* rows, int32_t n_rows, int32_t exact_act,
-                              int32_t n_threads, uint16_t* y_bf16, double* y64) {
+ORACLE_API int oracle_forward_ex(const oracle_layer* L, const uint16_t* x, int32_t T,
+                                 const int32_t* ids, const float* w,
+                                 const int32_t* rows, int32_t n_rows, int32_t exact_act,
+                                 const uint8_t* hq_in, const float* sh_in,
+                                 float* h32_out, uint8_t* hq_out, float* sh_out,
+                                 int32_t n_threads, uint16_t* y_bf16, double* y64) {
     if (!L || !x || !ids || !w) return -1;
     const int32_t H = L->H, I = L->I, E = L->E, k = L->k, SI = L->SI;
     if (H % QBLOCK || I % QBLOCK || (L->n_shared && SI % QBLOCK) || k < 1 || k > E || E > 1024) return -1;
@@ -352,10 +368,20 @@ ORACLE_API int oracle_forward(const oracle_layer* L, const uint16_t* x, int32_t 
             }
             if (!exact_act) oracle_quant_1x128(xf, H, xq, sx);
             for (int32_t h = 0; h < H; ++h) acc[h] = 0.0;
+            /* per (token, slot) h records: slots 0..k-1 routed (rank order), slot k shared */
+            const int32_t S = k + (L->n_shared ? 1 : 0);
+#define SLOT_IN(ptr, tok, slot, len) ((ptr) ? (ptr) + ((int64_t)(tok) * S + (slot)) * (len) : NULL)
+#define SLOT_OUT(slot) do { \
+                if (h32_out) memcpy(h32_out + ((int64_t)r * S + (slot)) * Imax, h32, sizeof(float) * (size_t)Imax); \
+                if (hq_out) memcpy(hq_out + ((int64_t)r * S + (slot)) * Imax, hq, (size_t)Imax); \
+                if (sh_out) memcpy(sh_out + ((int64_t)r * S + (slot)) * (Imax / QBLOCK), sh, sizeof(float) * (size_t)(Imax / QBLOCK)); \
+            } while (0)
             if (L->n_shared) {
                 expert_view sv = {L->sh_gate, L->sh_up, L->sh_down,
                                   L->sh_s_gate, L->sh_s_up, L->sh_s_down, H, SI};
-                expert_ffn(&sv, exact_act, xq, sx, xe, o, hbuf, h32, hq, sh);
+                expert_ffn(&sv, exact_act, xq, sx, xe, SLOT_IN(hq_in, t, k, Imax), SLOT_IN(sh_in, t, k, Imax / QBLOCK),
+                           o, hbuf, h32, hq, sh);
+                SLOT_OUT(k);
                 for (int32_t h = 0; h < H; ++h) acc[h] = o[h];
             }
             for (int32_t j = 0; j < k; ++j) {
@@ -367,9 +393,13 @@ ORACLE_API int oracle_forward(const oracle_layer* L, const uint16_t* x, int32_t 
                     L->s_gate + (int64_t)e * (I / QBLOCK) * (H / QBLOCK),
                     L->s_up + (int64_t)e * (I / QBLOCK) * (H / QBLOCK),
                     L->s_down + (int64_t)e * (H / QBLOCK) * (I / QBLOCK), H, I};
-                expert_ffn(&rv, exact_act, xq, sx, xe, o, hbuf, h32, hq, sh);
+                expert_ffn(&rv, exact_act, xq, sx, xe, SLOT_IN(hq_in, t, j, Imax), SLOT_IN(sh_in, t, j, Imax / QBLOCK),
+                           o, hbuf, h32, hq, sh);
+                SLOT_OUT(j);
                 for (int32_t h = 0; h < H; ++h) acc[h] += wj * o[h];
             }
+#undef SLOT_IN
+#undef SLOT_OUT
             for (int32_t h = 0; h < H; ++h) {
                 if (y64) y64[(int64_t)r * H + h] = acc[h];
                 if (y_bf16) y_bf16[(int64_t)r * H + h] = double_to_bf16(acc[h]);
@@ -391,6 +421,14 @@ ORACLE_API void oracle_e4m3_decode_n(const uint8_t* q, int64_t n, double* v) {
 }
 ORACLE_API void oracle_exp32_n(const float* x, int64_t n, float* y) {
     for (int64_t i = 0; i < n; ++i) y[i] = oracle_exp32(x[i]);
+}
+
+ORACLE_API int oracle_forward(const oracle_layer* L, const uint16_t* x, int32_t T,
+                              const int32_t* ids, const float* w,
+                              const int32_t* rows, int32_t n_rows, int32_t exact_act,
+                              int32_t n_threads, uint16_t* y_bf16, double* y64) {
+    return oracle_forward_ex(L, x, T, ids, w, rows, n_rows, exact_act, NULL, NULL, NULL, NULL, NULL,
+                             n_threads, y_bf16, y64);
 }
 
 ORACLE_API int oracle_threads(void) {

@@ -63,6 +63,12 @@ int     oracle_forward(const oracle_layer* L, const uint16_t* x_bf16, int32_t T,
                        const int32_t* ids, const float* w,
                        const int32_t* rows, int32_t n_rows, int32_t exact_act,
                        int32_t n_threads, uint16_t* y_bf16, double* y64);
+int     oracle_forward_ex(const oracle_layer* L, const uint16_t* x_bf16, int32_t T,
+                          const int32_t* ids, const float* w,
+                          const int32_t* rows, int32_t n_rows, int32_t exact_act,
+                          const uint8_t* hq_in, const float* sh_in,
+                          float* h32_out, uint8_t* hq_out, float* sh_out,
+                          int32_t n_threads, uint16_t* y_bf16, double* y64);
 int     oracle_threads(void);
 void    oracle_e4m3_encode_n(const float* v, int64_t n, uint8_t* q);
 void    oracle_e4m3_decode_n(const uint8_t* q, int64_t n, double* v);

@@ -44,6 +44,10 @@ def run_forward(layer: moe.Layer, x_bits: np.ndarray, mode: int, want_dbg: bool 
             "xq": torch.empty((T, H), dtype=torch.uint8, device="cuda"),
             "sx": torch.empty((T, H // 128), dtype=torch.float32, device="cuda"),
         }
+        S = k + layer.desc.n_shared
+        I = layer.desc.inter
+        bufs["hq"] = torch.empty((T, S, I), dtype=torch.uint8, device="cuda")
+        bufs["sh"] = torch.empty((T, S, I // 128), dtype=torch.float32, device="cuda")
         dbg = {n: t.data_ptr() for n, t in bufs.items()}
     ws, nbytes = layer.workspace(T, mode)
     fn = moe.moe_forward_prefill if mode == moe.MODE_PREFILL else moe.moe_forward_decode
@@ -128,3 +132,70 @@ def compare_y(y_gpu: np.ndarray, y_ref: np.ndarray):
 
 def oracle_y(inp: dict, k: int, ids, w, rows=None):
     return oracle.forward(inp, k, ids, w, rows=rows)
+
+
+def _e4m3_neighbours(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """True where codes a and b are adjacent values of the E4M3FN grid."""
+    va, vb = oracle.e4m3_decode(a), oracle.e4m3_decode(b)
+    lo, hi = np.minimum(va, vb), np.maximum(va, vb)
+    grid = np.unique(oracle.e4m3_decode(np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)))
+    return np.searchsorted(grid, hi) - np.searchsorted(grid, lo) == 1
+
+
+H_BAND = 1e-5       # band around an E4M3 rounding midpoint, as a fraction of the block amax
+SCALE_REL = 4e-6    # relative agreement of the h scales (amax / 448)
+
+
+def check_h_codes(gpu_hq, gpu_sh, ref: dict, max_frac: float = 1e-3):
+    """The GPU's h codes must equal the oracle's, except where the oracle's
+    h sits within H_BAND (of its 128-block's amax) of the rounding midpoint
+    between two adjacent E4M3 values: there the summation order decides and
+    either code is correct.  Scales (amax/448 per 128 values) within
+    SCALE_REL; at most max_frac of the codes may differ."""
+    h32, hq, sh = ref["h32"], ref["hq"], ref["sh"]
+    assert gpu_hq.shape == hq.shape and gpu_sh.shape == sh.shape
+    srel = np.abs(gpu_sh.astype(np.float64) - sh) / np.abs(sh)
+    diff = gpu_hq != hq
+    n = int(diff.sum())
+    dist = np.zeros(0)
+    if n:
+        ratio = (h32.astype(np.float64) / np.repeat(sh.astype(np.float64), 128, axis=-1))[diff]
+        va, vb = oracle.e4m3_decode(gpu_hq[diff]), oracle.e4m3_decode(hq[diff])
+        mid, step = 0.5 * (va + vb), np.abs(va - vb)
+        dist = np.abs(ratio - mid) / np.maximum(step, 1e-30)
+        hmag = np.abs(ratio) / 448.0
+    print(f"[h-codes] flips={n}/{hq.size} max_scale_rel={srel.max():.2e} "
+          f"max_dist/step={dist.max() if n else 0:.2e} "
+          f"flip |h|/amax: {np.array2string(hmag[:8], precision=3) if n else '-'}")
+    # The GPU forms h in fp32 from fp32 sums of 128-block partials, so its h
+    # carries an absolute error of order 1e-6 of the block's amax (the
+    # largest terms it sums); the oracle's h is fp64 rounded once.  A code
+    # may therefore differ only where the oracle's scaled value h/s (range
+    # +-448) lies within 448 * H_BAND of the midpoint between the two
+    # codes, and the 1x128 scales (amax/448) agree to SCALE_REL.
+    assert np.all(srel <= SCALE_REL), "h scales differ beyond rounding"
+    if n:
+        assert np.all(_e4m3_neighbours(gpu_hq[diff], hq[diff])), "an h code differs by more than one step"
+        assert np.all(np.abs(ratio - mid) <= 448.0 * H_BAND), "an h code differs away from a rounding boundary"
+    assert n <= max_frac * hq.size, f"{n} boundary flips out of {hq.size}"
+    return n
+
+
+def check_layer_output(inp: dict, k: int, dbg: dict, y_gpu: np.ndarray, rows=None):
+    """Layer parity.  1) The oracle, routed by the GPU's logits (dbg ids/w
+    were checked against oracle routing by the caller), evaluated on `rows`
+    with its own h: rel-L2 <= 5e-3.  2) Its h codes vs the GPU's: equal
+    except at rounding boundaries (check_h_codes).  3) The oracle evaluated
+    with the GPU's h codes (the valid alternative at those boundaries):
+    rel-L2 <= 5e-3 and max-abs <= 3e-2 * rms."""
+    ids, w = dbg["topk_ids"], dbg["topk_w"]
+    y_ref, href = oracle.forward(inp, k, ids, w, rows=rows, want_h=True)
+    sel = slice(None) if rows is None else rows
+    a = synth.bf16_to_f32(y_gpu[sel]).astype(np.float64)
+    b = synth.bf16_to_f32(y_ref).astype(np.float64)
+    rel_plain = np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30)
+    flips = check_h_codes(dbg["hq"][sel], dbg["sh"][sel], href)
+    y_ov = oracle.forward(inp, k, ids, w, rows=rows, hq_in=dbg["hq"], sh_in=dbg["sh"])
+    print(f"[parity] own-h rel_l2={rel_plain:.3e} h boundary flips={flips}")
+    assert rel_plain <= REL_L2_TOL, f"relative L2 error {rel_plain:.3e} > {REL_L2_TOL} (oracle's own h)"
+    return compare_y(y_gpu[sel], y_ov)

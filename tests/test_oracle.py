@@ -380,3 +380,33 @@ def test_oracle_thread_count_does_not_change_results(tiny_inputs):
     r = oracle.route_from_logits(L1, wl.top_k)
     assert np.array_equal(oracle.forward(inp, wl.top_k, r["ids"], r["w"], n_threads=1),
                           oracle.forward(inp, wl.top_k, r["ids"], r["w"], n_threads=3))
+
+
+def test_h_override_with_own_codes_is_identity_and_one_code_is_closed_form(tiny_inputs):
+    """The h-code override feeds given codes to the down projection: with the
+    oracle's own codes nothing changes; changing one code of one (token,
+    slot) moves y by exactly w * Wd[:, i] * (new - old) * s_block."""
+    wl, inp = tiny_inputs
+    k = wl.top_k
+    L = oracle.logits(inp["x"], inp["router_w"], inp["router_b"])
+    r = oracle.route_from_logits(L, k)
+    y, y64, hrec = oracle.forward(inp, k, r["ids"], r["w"], want_f64=True, want_h=True)
+    assert hrec["hq"].shape == (wl.T, k + 1, wl.inter)
+    # the recorded codes are the 1x128 quantisation of the recorded fp32 h
+    q, s = oracle.quant_1x128(hrec["h32"])
+    assert np.array_equal(q, hrec["hq"]) and np.array_equal(s, hrec["sh"])
+    y2, y64b = oracle.forward(inp, k, r["ids"], r["w"], want_f64=True, hq_in=hrec["hq"], sh_in=hrec["sh"])
+    assert np.array_equal(y64b, y64) and np.array_equal(y2, y)
+    t, j, i = 5, 1, 77                                        # token 5, routed slot 1, channel 77
+    hq = hrec["hq"].copy()
+    old = hq[t, j, i]
+    new = old + 1 if (old & 0x7F) < 0x7E else old - 1
+    hq[t, j, i] = new
+    _, y64c = oracle.forward(inp, k, r["ids"], r["w"], want_f64=True, hq_in=hq, sh_in=hrec["sh"])
+    e = r["ids"][t, j]
+    wd_col = oracle.e4m3_decode(inp["w_down"][e][:, i]) * np.repeat(inp["s_down"][e][:, i // 128].astype(np.float64), 128)
+    delta = (oracle.e4m3_decode(np.uint8(new)) - oracle.e4m3_decode(np.uint8(old))) * float(hrec["sh"][t, j, i // 128])
+    expect = float(r["w"][t, j]) * wd_col * delta
+    assert np.allclose(y64c[t] - y64[t], expect, rtol=1e-9, atol=1e-15)
+    others = np.arange(wl.T) != t
+    assert np.array_equal(y64c[others], y64[others])
