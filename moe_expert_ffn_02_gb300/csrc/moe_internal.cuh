@@ -229,6 +229,9 @@ cudaError_t launch_expert_down(const moe_layer* L, int T, const WsLayout& lay, c
                                cudaStream_t s);
 cudaError_t launch_h_gather(const moe_layer* L, int T, const WsLayout& lay, char* ws, uint8_t* hq_out, float* sh_out,
                             cudaStream_t s);
+int tc_tile_n();
+cudaError_t launch_expert_tc_gate_up(const moe_layer* L, int T, const WsLayout& lay, char* ws, cudaStream_t s);
+cudaError_t launch_expert_tc_down(const moe_layer* L, int T, const WsLayout& lay, char* ws, cudaStream_t s);
 cudaError_t launch_combine(const moe_layer* L, int T, const WsLayout& lay, char* ws, uint16_t* y, cudaStream_t s);
 cudaError_t launch_timeout_probe(const moe_layer* L, cudaStream_t s);
 }  // namespace moe

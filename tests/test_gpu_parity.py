@@ -130,10 +130,12 @@ def test_determinism_and_token_permutation(h):
     perm = np.random.default_rng(3).permutation(wl.T)
     yp, _ = h.run_forward(layer, inp["x"][perm], 1, want_dbg=False)
     assert np.array_equal(yp, y1[perm])
-    # decode and prefill entries compute the same function
+    # decode (weight-streaming mma.sync kernels) and prefill (tcgen05 kernels)
+    # compute the same function with different summation orders
     yd, _ = h.run_forward(layer, inp["x"][:64], 2, want_dbg=False)
     yq, _ = h.run_forward(layer, inp["x"][:64], 1, want_dbg=False)
-    assert np.array_equal(yd, yq)
+    a, b = synth.bf16_to_f32(yd).astype(np.float64), synth.bf16_to_f32(yq).astype(np.float64)
+    assert np.linalg.norm(a - b) / np.linalg.norm(b) <= h.REL_L2_TOL
     layer.close()
 
 
