@@ -155,6 +155,30 @@ moe_status moe_route(moe_layer* layer, const uint16_t* x, int32_t T, const moe_r
 moe_status moe_route_from_logits(moe_layer* layer, const float* logits, int32_t T,
                                  const moe_route_out* out, void* ws, size_t ws_bytes, void* stream);
 
+/* moe_route_from_logits without a workspace argument; this call allocates
+ * no memory.  The source pages have no counterpart: it exists for callers
+ * that cannot allocate device memory when they route -- serving runtimes
+ * that give all of HBM to their own pools at start-up and forbid cudaMalloc
+ * afterwards (which would also synchronise the device mid-step), and plain
+ * C callers without an allocator to carve a workspace from.
+ * Its scratch is a fixed array of MOE_NOALLOC_SCRATCH_BYTES (4 MiB) compiled
+ * into the library; every GPU that loads the library holds it until the
+ * process exits.  Outputs go to `out` exactly as moe_route_from_logits
+ * writes them (same kernels, bit-identical results).
+ *  - Size limit: the routing scratch for (T, n_experts, top_k) must fit the
+ *    array -- roughly 160 bytes per token at E = 256, k = 8 (T <= ~26,000) --
+ *    otherwise MOE_ERR_UNSUPPORTED is returned and nothing runs.
+ *  - Set-up: the first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture on the device.
+ *  - Sharing: every call uses the same array, which keeps the previous
+ *    call's contents; every scratch word a call reads is first written by
+ *    that call, so nothing needs clearing.  Calls that overlap on the GPU
+ *    (other streams, other host threads) race on the array: serialise them. */
+#define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+moe_status moe_route_from_logits_noalloc(moe_layer* layer, const float* logits, int32_t T,
+                                         const moe_route_out* out, void* stream);
+
 /* The whole layer for a prefill batch: x [T][H] bf16 -> y [T][H] bf16.
  * `dbg` (nullable) receives the routing, exactly as moe_route would write it.
  * T = 0 is a valid no-op. */

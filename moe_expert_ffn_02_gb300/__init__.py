@@ -20,7 +20,7 @@ from . import build as _build
 __all__ = [
     "MoeError", "MoeDesc", "MoeWeights", "MoeRouteOut", "MODE_ROUTE", "MODE_PREFILL", "MODE_DECODE",
     "DECODE_MAX_T", "moe_create", "moe_destroy", "moe_workspace_bytes", "moe_route", "moe_route_from_logits",
-    "moe_forward_prefill", "moe_forward_decode", "moe_forward_host", "moe_get_device_status",
+    "moe_route_from_logits_noalloc", "moe_forward_prefill", "moe_forward_decode", "moe_forward_host", "moe_get_device_status",
     "moe_set_wait_limit", "moe_debug_timeout_probe", "moe_profile_enable", "moe_profile_read", "moe_status_string", "moe_last_error",
     "moe_abi_version", "library_path", "load", "Layer",
 ]
@@ -89,6 +89,7 @@ def load(build_if_missing: bool = False):
             "moe_get_device_status": ([vp, vp, ctypes.POINTER(u32)], st),
             "moe_set_wait_limit": ([vp, u32], st),
             "moe_debug_timeout_probe": ([vp, vp], st),
+            "moe_route_from_logits_noalloc": ([vp, vp, i32, ctypes.POINTER(MoeRouteOut), vp], st),
             "moe_profile_enable": ([vp, i32], st),
             "moe_profile_read": ([vp, ctypes.POINTER(ctypes.c_float), i32], st),
             "moe_status_string": ([st], ctypes.c_char_p),
@@ -153,6 +154,13 @@ def moe_route(layer: int, x: int, T: int, out, ws: int, ws_bytes: int, stream: i
 
 def moe_route_from_logits(layer: int, logits: int, T: int, out, ws: int, ws_bytes: int, stream: int = 0) -> None:
     _check(load().moe_route_from_logits(layer, logits, T, _route_out(out), ws, ws_bytes, stream))
+
+
+def moe_route_from_logits_noalloc(layer: int, logits: int, T: int, out, stream: int = 0) -> None:
+    """Routing from given logits with the library's built-in scratch (no
+    workspace, no allocation) -- for callers that cannot allocate device
+    memory when they route.  See include/moe.h for the size limit."""
+    _check(load().moe_route_from_logits_noalloc(layer, logits, T, _route_out(out), stream))
 
 
 def moe_forward_prefill(layer: int, x: int, T: int, y: int, dbg, ws: int, ws_bytes: int, stream: int = 0) -> None:

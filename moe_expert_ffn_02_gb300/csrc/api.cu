@@ -175,6 +175,10 @@ moe_status run_forward(moe_layer* L, int mode, const uint16_t* x, int T, uint16_
 
 }  // namespace
 
+namespace moe {
+void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
+}  // namespace moe
+
 MOE_EXPORT int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
 
 MOE_EXPORT const char* moe_last_error(void) { return g_last_error.c_str(); }

@@ -234,4 +234,5 @@ cudaError_t launch_expert_tc_gate_up(const moe_layer* L, int T, const WsLayout& 
 cudaError_t launch_expert_tc_down(const moe_layer* L, int T, const WsLayout& lay, char* ws, cudaStream_t s);
 cudaError_t launch_combine(const moe_layer* L, int T, const WsLayout& lay, char* ws, uint16_t* y, cudaStream_t s);
 cudaError_t launch_timeout_probe(const moe_layer* L, cudaStream_t s);
+void set_last_error(const char* msg);   // message returned by moe_last_error()
 }  // namespace moe
