@@ -61,13 +61,14 @@ def library_path() -> str:
 
 
 def load(build_if_missing: bool = False):
-    """Load libmoe.so (optionally building it first)."""
+    """Load libmoe.so (optionally building it first).  The environment
+    variable MOE_LIBRARY, if set, names another build of the library to load."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
-        path = _build.LIB
-        if build_if_missing and not _build.up_to_date():
+        path = os.environ.get("MOE_LIBRARY") or _build.LIB
+        if build_if_missing and path == _build.LIB and not _build.up_to_date():
             _build.build()
         if not os.path.exists(path):
             raise MoeError(-1, f"libmoe.so is not built ({path}); run __graft_entry__.build() first")

@@ -1,49 +1,51 @@
 // Grouped FP8 expert GEMMs for prefill on the 5th-generation tensor cores
 // (tcgen05, sm_103a).
 //
-// Swap-AB tiles: A = 128 rows of an expert's weight matrix (output
-// features), B = 128 token rows of the expert's group, K = 128 per stage.
-// Both operands are 16 KB 128-byte-swizzled K-major images in global memory
-// (weight tiles repacked at load time; activation tiles written so by the
-// quantiser / gate-up epilogue), so the producer warp moves each with one
-// bulk copy.  One thread of the MMA warp issues tcgen05.mma kind::f8f6f4
-// (E4M3 x E4M3, fp32 accumulate in tensor memory) -- 4 instructions of
-// K = 32 per stage, two accumulators (gate, up) in the gate/up kernel --
-// and commits to mbarriers.  Accumulators are double-buffered in TMEM so
-// the tensor core works on block kb+1 while the epilogue warps promote
-// block kb.
+// Tile: A = 128 token rows of one expert's group, B = 256 weight rows, K =
+// 128 per stage.  Gate/up: B = the expert's gate tile and up tile of the
+// same 128 inner features, which sit next to each other in the repacked
+// weights, so one M128 x N256 x K32 MMA covers both projections.  Down: B =
+// two consecutive 128-row tiles of the down weights (256 outputs).  Both
+// operands are 128-byte-swizzled K-major images that one bulk copy each
+// brings into shared memory.  One thread issues tcgen05.mma kind::f8f6f4
+// (E4M3 x E4M3, fp32 accumulate in tensor memory), 4 per stage, with
+// descriptors advanced by a constant; accumulators are double-buffered in
+// TMEM (2 x 256 columns).
 //
 // Scale promotion (FP8 GEMV section of the CPU-GPU hybrid inference
-// article, Fig. 9-10: block partial sums are scaled once per 128-element
-// block): every K block's partial D_kb is read out of TMEM (tcgen05.ld) and
-// added as acc += D_kb * s_w[kb] * s_x[token][kb] in fp32 registers.
+// article, Fig. 9-10: a 128-element block's partial sum is scaled once):
+// each TMEM lane is one token, so its activation scale s_x[token][kb] is a
+// per-thread scalar and the weight scales s_w[kb] are uniform; the epilogue
+// warps read each block's partial with tcgen05.ld and promote it with packed
+// fp32x2 FMAs into registers.  Gate/up then forms h = SiLU(g)*u and its
+// 1x128 E4M3 codes (the activation and elementwise product between gate/up
+// and down, "CPU fine-grained parallelism" section of the same article);
+// down writes fp32 output rows.
 //
-// Unit = (group, m tile, n tile), n fastest, so the n tiles of one weight
-// row block run on neighbouring CTAs and share its bytes through L2.
+// Unit = (group, token tile of 128, weight block), weight block fastest, so
+// the CTAs working on one token tile at a time share its bytes through L2.
 #include "moe_internal.cuh"
 
 namespace moe {
 namespace tc {
 
-constexpr int BM = 128;                 // weight rows per tile (TMEM lanes)
-constexpr int BN = 128;                 // tokens per tile (TMEM columns per accumulator)
+constexpr int BM = 128;                 // token rows per tile (TMEM lanes)
+constexpr int BN = 256;                 // weight rows per tile (TMEM columns per buffer)
 constexpr int EPI_WARPS = 8;            // 4 lane quarters x 2 column halves
-constexpr int COLS = BN / 2;            // columns per epilogue thread
-constexpr int NTHREADS = (2 + EPI_WARPS) * 32;
+constexpr int HALF = BN / 2;            // columns per epilogue thread (per buffer)
+constexpr int CTRL_WARPS = 4;           // warpgroup 0: producer, MMA issuer, 2 idle
+constexpr int NTHREADS = (CTRL_WARPS + EPI_WARPS) * 32;
+// Register split (setmaxnreg acts per warpgroup): launched at 168 per thread
+// (384 x 168 = 64,512); the control warpgroup drops to 32 and the two
+// epilogue warpgroups rise to 232: 4*32*32 + 8*32*232 = 63,488.
+constexpr int CTRL_REGS = 32, EPI_REGS = 232;
+static_assert(CTRL_WARPS * 32 * CTRL_REGS + EPI_WARPS * 32 * EPI_REGS <= NTHREADS * 168, "register split");
 constexpr uint32_t TMEM_COLS = 512;
-
-template <bool GU>
-struct Cfg {
-    static constexpr int W_BYTES = GU ? 2 * TILE_BYTES : TILE_BYTES;
-    static constexpr int X_BYTES = BN * 128;
-    static constexpr int STAGE = W_BYTES + X_BYTES;
-    static constexpr int STAGES = GU ? 4 : 6;
-    static constexpr int NACC = GU ? 2 : 1;
-    static constexpr int BUF_COLS = NACC * BN;          // TMEM columns per buffer
-    static constexpr int SCALE_BYTES = EPI_WARPS * 2 * NACC * COLS * 4;
-    static constexpr int STAGING = GU ? BN * 144 + 2 * 4 * COLS * 4 : 0;
-    static constexpr int SMEM = STAGES * STAGE + SCALE_BYTES + STAGING + 256;
-};
+constexpr int STAGES = 4;
+constexpr int W_BYTES = 2 * TILE_BYTES;   // 256 weight rows
+constexpr int X_BYTES = BM * 128;         // 128 token rows
+constexpr int STAGE = W_BYTES + X_BYTES;
+constexpr int SMEM = STAGES * STAGE + 2 * 4 * 32 * 4 + 256;   // + amax exchange
 
 struct Args {
     const uint8_t* w;         // tile images of all groups
@@ -51,7 +53,7 @@ struct Args {
     const uint8_t* act;       // [K/128][rows_pad][128] swizzled E4M3
     const float* actsT;       // [K/128][rows_pad]
     int ld;                   // rows_pad
-    int K, M;
+    int K, M;                 // reduction length; output features (I or H)
     const GroupTable* gt;
     uint8_t* hq;              // gate/up output codes (same layout as act)
     float* shT;               // gate/up output scales
@@ -61,24 +63,24 @@ struct Args {
 };
 
 struct Unit {
-    int expert, mb, row_begin, valid;
+    int expert, wb, row_begin, valid;
 };
 
-// u -> (group, m tile, n tile) with n fastest inside a group.
-__device__ __forceinline__ Unit decode_unit(const GroupTable* gt, int u, int MT) {
-    int lo = 0, hi = gt->n_groups - 1;            // last group with MT * pair_start <= u
+// u -> (group, token tile, weight block) with the weight block fastest.
+// NB = weight blocks per group (I/128 for gate/up, ceil(H/256) for down).
+__device__ __forceinline__ Unit decode_unit(const GroupTable* gt, int u, int NB) {
+    const int pair = u / NB;
+    Unit r;
+    r.wb = u - pair * NB;
+    int lo = 0, hi = gt->n_groups - 1;            // last group with pair_start <= pair
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (gt->pair_start[mid] * MT <= u) lo = mid; else hi = mid - 1;
+        if (gt->pair_start[mid] <= pair) lo = mid; else hi = mid - 1;
     }
-    const int nt_g = gt->pair_start[lo + 1] - gt->pair_start[lo];
-    const int local = u - gt->pair_start[lo] * MT;
-    const int mb = local / nt_g, nt = local - mb * nt_g;
-    Unit r;
+    const int nt = pair - gt->pair_start[lo];
     r.expert = gt->expert[lo];
-    r.mb = mb;
-    r.row_begin = gt->row0[lo] + nt * BN;
-    r.valid = min(BN, gt->rows[lo] - nt * BN);
+    r.row_begin = gt->row0[lo] + nt * BM;
+    r.valid = min(BM, gt->rows[lo] - nt * BM);
     return r;
 }
 
@@ -98,25 +100,27 @@ __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence:
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row atoms
-// 1024 B apart (stride byte offset), descriptor version 1.
+// 1024 B apart (stride byte offset), descriptor version 1.  The start
+// address occupies the low 14 bits (bytes >> 4), so stepping K by 32 bytes
+// inside the swizzle atom adds 2.
+constexpr uint64_t DESC_HI = ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) |
+                             ((uint64_t)2 << 61);
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)1 << 16;                 // leading byte offset (unused for swizzled K-major)
-    d |= (uint64_t)(1024 >> 4) << 32;       // stride byte offset
-    d |= (uint64_t)1 << 46;                 // version
-    d |= (uint64_t)2 << 61;                 // 128-byte swizzle
-    return d;
+    return DESC_HI | (uint64_t)((saddr & 0x3FFFFu) >> 4);
 }
 
-// Instruction descriptor, kind::f8f6f4: D f32, A = B = E4M3, both K-major.
-constexpr uint32_t IDESC = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                           ((uint32_t)(BM >> 4) << 24);
+// Instruction descriptor, kind::f8f6f4: D f32, A = B = E4M3, both K-major,
+// M = 128, N = n.
+__device__ __forceinline__ uint32_t idesc_for(int n) {
+    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
 
-__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate) {
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(IDESC), "r"(accumulate)
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -125,9 +129,8 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                  : "memory");
 }
 
-// 32 lanes x 32 columns of fp32 (one register per column per thread).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
+// 32 lanes x 32 columns, raw 32-bit words (one register per column per thread).
+__device__ __forceinline__ void tmem_ld32u(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
         "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
@@ -137,34 +140,46 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr)
         : "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Packed fp32 pairs: acc += p * c on two lanes with one fma.rn.f32x2, each
+// lane rounded exactly like fmaf.  Accumulators stay packed for a whole unit.
+__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ void fma2(uint64_t& acc, uint64_t p, uint64_t c) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(p), "l"(c));
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
 
 // ------------------------------------------------------------------ kernel
 template <bool GU>
 __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
-    using C = Cfg<GU>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
-    float* scl = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE);           // [EPI_WARPS][2][NACC][COLS]
-    uint8_t* staging = smem + C::STAGES * C::STAGE + C::SCALE_BYTES;               // gate/up: codes + amax
-    __shared__ uint64_t full[C::STAGES], empty[C::STAGES], tfull[2], tempty[2];
+    float* amax_x = reinterpret_cast<float*>(smem + STAGES * STAGE);   // [2 halves][4 quarters][32 lanes]
+    __shared__ uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int MT = a.M / QB, KT = a.K / QB;
+    const int KT = a.K / QB;
+    const int MT128 = a.M / QB;                              // 128-row weight tiles per expert
+    const int NB = GU ? MT128 : (MT128 + 1) / 2;             // weight blocks per unit row
     const GroupTable* gt = a.gt;
-    const int n_units = gt->n_pairs * MT;
+    const int n_units = gt->n_pairs * NB;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
         for (int b = 0; b < 2; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], EPI_WARPS); }
         fence_mbar_init();
         abort_flag = 0;
@@ -176,40 +191,53 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
     const uint32_t tmem = tmem_slot;
     volatile int* abort = &abort_flag;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
+    if (warp < CTRL_WARPS) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CTRL_REGS));
+        if (warp == 0 && lane == 0) {
+            // -------------------------------------------------------- producer
             int stage = 0;
             uint32_t phase = 0, armed = 0, armed_par = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                const Unit un = decode_unit(gt, u, MT);
-                const uint8_t* wbase = a.w + ((size_t)(un.expert * MT + un.mb) * KT) * C::W_BYTES;
+                const Unit un = decode_unit(gt, u, NB);
+                // gate/up: the gate+up pair of inner tile wb (32 KB, contiguous per k block);
+                // down: tiles 2wb and 2wb+1 of the output rows (16 KB each, KT tiles apart)
+                const int t0 = GU ? un.wb : 2 * un.wb;
+                const bool two = GU || (t0 + 1 < MT128);
+                const uint32_t wbytes = two ? (uint32_t)W_BYTES : (uint32_t)TILE_BYTES;
+                const uint8_t* wbase = a.w + ((size_t)(un.expert * MT128 + t0) * KT) * (GU ? W_BYTES : TILE_BYTES);
                 for (int kb = 0; kb < KT; ++kb) {
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, a.wait_limit, a.status, abort)) {
                         ok = false;
                         break;
                     }
-                    uint8_t* st = stages + stage * C::STAGE;
-                    mbar_arrive_expect_tx(&full[stage], C::STAGE);
-                    bulk_g2s(st, wbase + (size_t)kb * C::W_BYTES, C::W_BYTES, &full[stage]);
-                    bulk_g2s(st + C::W_BYTES, a.act + act_offset(kb, un.row_begin, a.ld), C::X_BYTES, &full[stage]);
+                    uint8_t* st = stages + stage * STAGE;
+                    mbar_arrive_expect_tx(&full[stage], wbytes + X_BYTES);
+                    if (GU) {
+                        bulk_g2s(st, wbase + (size_t)kb * W_BYTES, W_BYTES, &full[stage]);
+                    } else {
+                        bulk_g2s(st, wbase + (size_t)kb * TILE_BYTES, TILE_BYTES, &full[stage]);
+                        if (two)
+                            bulk_g2s(st + TILE_BYTES, wbase + ((size_t)KT + kb) * TILE_BYTES, TILE_BYTES, &full[stage]);
+                    }
+                    bulk_g2s(st + W_BYTES, a.act + act_offset(kb, un.row_begin, a.ld), X_BYTES, &full[stage]);
                     armed |= 1u << stage;
                     armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-                    if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
             }
-            for (int s = 0; s < C::STAGES; ++s)
+            for (int s = 0; s < STAGES; ++s)
                 if ((armed >> s) & 1u) mbar_wait_bounded(&full[s], (armed_par >> s) & 1u, a.wait_limit, a.status, nullptr);
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        } else if (warp == 1 && lane == 0) {
+            // -------------------------------------------------------- MMA issuer
             int stage = 0, buf = 0;
             uint32_t phase = 0, tphase = 0;
             bool ok = true;
+            const uint64_t d0 = sw128_desc(smem_addr(stages));        // stage 0, weight operand
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                const int wb = u % NB;
+                const bool two = GU || (2 * wb + 1 < MT128);
+                const uint32_t idesc = idesc_for(two ? BN : BN / 2);
                 for (int kb = 0; kb < KT; ++kb) {
                     if (!mbar_wait_bounded(&tempty[buf], tphase ^ 1u, a.wait_limit, a.status, abort) ||
                         !mbar_wait_bounded(&full[stage], phase, a.wait_limit, a.status, abort)) {
@@ -217,128 +245,156 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sW = smem_addr(stages + stage * C::STAGE);
-                    const uint32_t sX = sW + C::W_BYTES;
-                    const uint32_t d0 = tmem + (uint32_t)(buf * C::BUF_COLS);
-#pragma unroll
-                    for (int k = 0; k < QB / 32; ++k) {
-                        const uint64_t bdesc = sw128_desc(sX + k * 32);
-                        mma_f8(d0, sw128_desc(sW + k * 32), bdesc, k > 0);
-                        if (GU) mma_f8(d0 + BN, sw128_desc(sW + TILE_BYTES + k * 32), bdesc, k > 0);
-                    }
+                    const uint64_t bdesc = d0 + (uint64_t)((stage * STAGE) >> 4);                   // weights
+                    const uint64_t adesc = d0 + (uint64_t)((stage * STAGE + W_BYTES) >> 4);       // tokens
+                    const uint32_t dt = tmem + (uint32_t)(buf * BN);
+                    mma_f8(dt, adesc, bdesc, idesc, 0u);
+                    mma_f8(dt, adesc + 2, bdesc + 2, idesc, 1u);
+                    mma_f8(dt, adesc + 4, bdesc + 4, idesc, 1u);
+                    mma_f8(dt, adesc + 6, bdesc + 6, idesc, 1u);
                     mma_commit(&empty[stage]);
                     mma_commit(&tfull[buf]);
-                    if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                     if (++buf == 2) { buf = 0; tphase ^= 1u; }
                 }
             }
         }
         __syncwarp();
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(EPI_REGS));
         // ------------------------------------------------------------ epilogue warps
-        const int ew = warp - 2;                  // 0..7
-        const int quarter = warp & 3;             // TMEM lanes this warp may read
-        const int half = ew >> 2;                 // column half
-        const int row = quarter * 32 + lane;      // output feature within the tile
-        float* my_scl = scl + ew * (2 * C::NACC * COLS);
+        const int ew = warp - CTRL_WARPS;           // 0..7
+        const int quarter = warp & 3;               // TMEM lanes this warp may read
+        const int half = ew >> 2;                   // column half of the 256-column buffer
+        const int r = quarter * 32 + lane;          // token row inside the tile
         int buf = 0;
         uint32_t tphase = 0;
         bool dead = false;
         for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-            const Unit un = decode_unit(gt, u, MT);
-            const float* wsc = a.wscale + ((size_t)(un.expert * MT + un.mb) * KT) * C::NACC;
-            float acc[C::NACC][COLS];
+            const Unit un = decode_unit(gt, u, NB);
+            const bool rv = r < un.valid;
+            const size_t arow = (size_t)un.row_begin + r;
+            const int t0 = GU ? un.wb : 2 * un.wb;
+            const bool two = GU || (t0 + 1 < MT128);
+            // weight scales: gate/up j = 0 gate, 1 up; down: my half's tile (t0 + half)
+            const float* ws0 = GU ? a.wscale + ((size_t)(un.expert * MT128 + t0) * KT) * 2
+                                  : a.wscale + ((size_t)(un.expert * MT128 + t0 + ((half && two) ? 1 : 0)) * KT);
+            float wreg[2][2];                          // blocks lane and lane + 32
 #pragma unroll
-            for (int j = 0; j < C::NACC; ++j)
+            for (int j = 0; j < 2; ++j)
 #pragma unroll
-                for (int c = 0; c < COLS; ++c) acc[j][c] = 0.f;
-            // prefetch the activation scales of block 0 for this lane's two columns
-            const int col0 = half * COLS + lane, col1 = col0 + 32;
-            float sx0 = (col0 < un.valid) ? __ldg(a.actsT + un.row_begin + col0) : 0.f;
-            float sx1 = (col1 < un.valid) ? __ldg(a.actsT + un.row_begin + col1) : 0.f;
-            for (int kb = 0; kb < KT; ++kb) {
-                // combined scale per column: s_w[kb] * s_x[col][kb]
-                float* cs = my_scl + (kb & 1) * (C::NACC * COLS);
-#pragma unroll
-                for (int j = 0; j < C::NACC; ++j) {
-                    const float sw = __ldg(wsc + (size_t)kb * C::NACC + j);
-                    cs[j * COLS + lane] = sw * sx0;
-                    cs[j * COLS + lane + 32] = sw * sx1;
+                for (int i = 0; i < 2; ++i) {
+                    const int kb = lane + 32 * i;
+                    float v = 0.f;
+                    if (kb < KT && (GU || j == 0)) v = GU ? __ldg(ws0 + (size_t)kb * 2 + j) : __ldg(ws0 + kb);
+                    wreg[j][i] = v;
                 }
-                if (kb + 1 < KT) {
-                    sx0 = (col0 < un.valid) ? __ldg(a.actsT + (size_t)(kb + 1) * a.ld + un.row_begin + col0) : 0.f;
-                    sx1 = (col1 < un.valid) ? __ldg(a.actsT + (size_t)(kb + 1) * a.ld + un.row_begin + col1) : 0.f;
-                }
-                __syncwarp();
-                if (!dead && !mbar_wait_bounded(&tfull[buf], tphase, a.wait_limit, a.status, abort)) dead = true;
-                if (!dead) {
-                    tc_fence_after();
-                    const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * C::BUF_COLS) +
-                                           (uint32_t)(half * COLS);
+            uint64_t acc[HALF / 2];                   // 128 fp32 accumulators, packed in pairs
 #pragma unroll
-                    for (int j = 0; j < C::NACC; ++j) {
+            for (int c = 0; c < HALF / 2; ++c) acc[c] = 0ull;
+            constexpr int SXD = 4;                    // activation-scale prefetch distance (blocks)
+            float sxr[SXD];
 #pragma unroll
-                        for (int ch = 0; ch < COLS / 32; ++ch) {
-                            float p[32];
-                            tmem_ld32(tbase + (uint32_t)(j * BN + ch * 32), p);
+            for (int d = 0; d < SXD; ++d) sxr[d] = (rv && d < KT) ? __ldg(a.actsT + (size_t)d * a.ld + arow) : 0.f;
+            for (int kb0 = 0; kb0 < KT; kb0 += SXD) {
+#pragma unroll
+                for (int d = 0; d < SXD; ++d) {
+                    const int kb = kb0 + d;
+                    if (kb >= KT) break;
+                    // per-thread combined scales for this block: s_w[j][kb] * s_x[token][kb]
+                    float cj[2];
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        float sw;
+                        if (KT <= 64) sw = __shfl_sync(0xFFFFFFFFu, kb < 32 ? wreg[j][0] : wreg[j][1], kb & 31);
+                        else sw = (GU || j == 0) ? (GU ? __ldg(ws0 + (size_t)kb * 2 + j) : __ldg(ws0 + kb)) : 0.f;
+                        cj[j] = sw * sxr[d];
+                    }
+                    if (kb + SXD < KT) sxr[d] = rv ? __ldg(a.actsT + (size_t)(kb + SXD) * a.ld + arow) : 0.f;
+                    if (!dead && !mbar_wait_bounded(&tfull[buf], tphase, a.wait_limit, a.status, abort)) dead = true;
+                    if (!dead) {
+                        tc_fence_after();
+                        const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN);
+                        // two TMEM round trips of 64 columns each
+#pragma unroll
+                        for (int ch = 0; ch < 2; ++ch) {
+                            uint32_t pv[2][32];
+                            if (GU) {
+                                // gate cols [64h + 32ch, +32) and up cols [128 + 64h + 32ch, +32)
+                                tmem_ld32u(tb + (uint32_t)(64 * half + 32 * ch), pv[0]);
+                                tmem_ld32u(tb + (uint32_t)(128 + 64 * half + 32 * ch), pv[1]);
+                            } else {
+                                tmem_ld32u(tb + (uint32_t)(128 * half + 64 * ch), pv[0]);
+                                tmem_ld32u(tb + (uint32_t)(128 * half + 64 * ch + 32), pv[1]);
+                            }
                             tmem_wait_ld();
 #pragma unroll
-                            for (int c4 = 0; c4 < 8; ++c4) {
-                                const float4 s4 = *reinterpret_cast<const float4*>(cs + j * COLS + ch * 32 + c4 * 4);
-                                acc[j][ch * 32 + c4 * 4 + 0] = __fmaf_rn(p[c4 * 4 + 0], s4.x, acc[j][ch * 32 + c4 * 4 + 0]);
-                                acc[j][ch * 32 + c4 * 4 + 1] = __fmaf_rn(p[c4 * 4 + 1], s4.y, acc[j][ch * 32 + c4 * 4 + 1]);
-                                acc[j][ch * 32 + c4 * 4 + 2] = __fmaf_rn(p[c4 * 4 + 2], s4.z, acc[j][ch * 32 + c4 * 4 + 2]);
-                                acc[j][ch * 32 + c4 * 4 + 3] = __fmaf_rn(p[c4 * 4 + 3], s4.w, acc[j][ch * 32 + c4 * 4 + 3]);
+                            for (int j = 0; j < 2; ++j) {
+                                // gate/up: j = 0 gate, 1 up (scales cj[0], cj[1]); down: one scale per half
+                                const float c = GU ? cj[j] : cj[0];
+                                const uint64_t cc = pack2(__float_as_uint(c), __float_as_uint(c));
+                                const int base = GU ? (j * 32 + ch * 16) : (ch * 32 + j * 16);
+#pragma unroll
+                                for (int q = 0; q < 16; ++q)
+                                    fma2(acc[base + q], pack2(pv[j][2 * q], pv[j][2 * q + 1]), cc);
                             }
                         }
+                        tc_fence_before();
                     }
-                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty[buf]);
+                    if (++buf == 2) { buf = 0; tphase ^= 1u; }
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[buf]);
-                if (++buf == 2) { buf = 0; tphase ^= 1u; }
             }
 
             if (GU) {
-                // -------------------------------------- SiLU(g)*u and 1x128 E4M3 quantisation of h
-                uint8_t* qst = staging;                                         // [BN][144]
-                float* amax_s = reinterpret_cast<float*>(staging + BN * 144);   // [2 halves][4 quarters][COLS]
-                float* h = acc[0];
+                // ------------------------------------------ SiLU(g)*u, 1x128 E4M3 quantisation of h
+                // this thread: features [64h, 64h+64) of the 128-feature tile; gate in acc[0..31],
+                // up in acc[32..63]
+                float h[64];
+                float amax = 0.f;
 #pragma unroll
-                for (int c = 0; c < COLS; ++c) h[c] = silu_mul(acc[0][c], acc[GU ? 1 : 0][c]);
-#pragma unroll
-                for (int c = 0; c < COLS; ++c) {
-                    float m = fabsf(h[c]);
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-                    if (lane == 0) amax_s[(half * 4 + quarter) * COLS + c] = m;
+                for (int q = 0; q < 32; ++q) {
+                    float g0, g1, u0, u1;
+                    unpack2(acc[q], g0, g1);
+                    unpack2(acc[32 + q], u0, u1);
+                    h[2 * q] = silu_mul(g0, u0);
+                    h[2 * q + 1] = silu_mul(g1, u1);
+                    amax = fmaxf(amax, fmaxf(fabsf(h[2 * q]), fabsf(h[2 * q + 1])));
                 }
+                amax_x[(half * 4 + quarter) * 32 + lane] = amax;
                 named_bar_sync(1, EPI_WARPS * 32);
+                const float mx = fmaxf(amax, amax_x[((1 - half) * 4 + quarter) * 32 + lane]);
+                const float sc = (mx > 0.f) ? __fdiv_rn(mx, 448.0f) : 1.0f;
+                if (rv) {
+                    uint8_t* dst = a.hq + act_offset(un.wb, un.row_begin + r, a.ld);
 #pragma unroll
-                for (int c = 0; c < COLS; ++c) {
-                    const float* am = amax_s + half * 4 * COLS + c;
-                    const float mx = fmaxf(fmaxf(am[0], am[COLS]), fmaxf(am[2 * COLS], am[3 * COLS]));
-                    const float sc = (mx > 0.f) ? __fdiv_rn(mx, 448.0f) : 1.0f;
-                    const uint16_t q2 = f32x2_to_e4m3x2(__fdiv_rn(h[c], sc), 0.f);
-                    qst[(half * COLS + c) * 144 + row] = (uint8_t)(q2 & 0xFF);
-                    if (quarter == 0 && lane == 0 && half * COLS + c < un.valid)
-                        a.shT[(size_t)un.mb * a.ld + un.row_begin + half * COLS + c] = sc;
-                }
-                named_bar_sync(1, EPI_WARPS * 32);
-                const int tid = threadIdx.x - 64;
-                for (int rr = tid >> 3; rr < un.valid; rr += (EPI_WARPS * 32) >> 3) {
-                    const uint4 v = lds128(qst + rr * 144 + (tid & 7) * 16);
-                    const int pos = (tid & 7) ^ (rr & 7);
-                    *reinterpret_cast<uint4*>(a.hq + act_offset(un.mb, un.row_begin + rr, a.ld) + pos * 16) = v;
+                    for (int c4 = 0; c4 < 4; ++c4) {                 // 16-byte chunks 4h .. 4h+3
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int e = c4 * 16 + k * 4;
+                            w4[k] = pack4_e4m3(__fdiv_rn(h[e], sc), __fdiv_rn(h[e + 1], sc), __fdiv_rn(h[e + 2], sc),
+                                               __fdiv_rn(h[e + 3], sc));
+                        }
+                        const int chunk = (half * 4 + c4) ^ (r & 7);     // row_begin is a multiple of 8
+                        *reinterpret_cast<uint4*>(dst + chunk * 16) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                    if (half == 0) a.shT[(size_t)un.wb * a.ld + un.row_begin + r] = sc;
                 }
                 named_bar_sync(1, EPI_WARPS * 32);
             } else {
-                // -------------------------------------- fp32 expert output rows
-                const int cbeg = half * COLS;
+                // ------------------------------------------ fp32 expert output row: 128 features
+                if (rv && (half == 0 || two)) {
+                    float* dst = a.out + arow * a.M + (size_t)un.wb * BN + half * HALF;
 #pragma unroll
-                for (int c = 0; c < COLS; ++c)
-                    if (cbeg + c < un.valid)
-                        a.out[(size_t)(un.row_begin + cbeg + c) * a.M + un.mb * QB + row] = acc[0][c];
+                    for (int q = 0; q < HALF / 4; ++q) {
+                        float v0, v1, v2, v3;
+                        unpack2(acc[2 * q], v0, v1);
+                        unpack2(acc[2 * q + 1], v2, v3);
+                        *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(v0, v1, v2, v3);
+                    }
+                }
             }
         }
     }
@@ -350,11 +406,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
 
 template <bool GU>
 static cudaError_t launch(const moe_layer* L, const WsLayout& lay, char* ws, cudaStream_t s) {
-    using C = Cfg<GU>;
     static bool attr[2] = {false, false};
     if (!attr[GU]) {
-        cudaError_t e = cudaFuncSetAttribute(expert_tc_kernel<GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::SMEM + 1024);
+        cudaError_t e =
+            cudaFuncSetAttribute(expert_tc_kernel<GU>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM + 1024);
         if (e != cudaSuccess) return e;
         attr[GU] = true;
     }
@@ -378,13 +433,13 @@ static cudaError_t launch(const moe_layer* L, const WsLayout& lay, char* ws, cud
         a.actsT = reinterpret_cast<const float*>(ws + lay.shT);
         a.K = I; a.M = H;
     }
-    expert_tc_kernel<GU><<<L->num_sms, NTHREADS, C::SMEM + 1024, s>>>(a);
+    expert_tc_kernel<GU><<<L->num_sms, NTHREADS, SMEM + 1024, s>>>(a);
     return cudaGetLastError();
 }
 
 }  // namespace tc
 
-int tc_tile_n() { return tc::BN; }
+int tc_tile_n() { return tc::BM; }
 
 cudaError_t launch_expert_tc_gate_up(const moe_layer* L, int T, const WsLayout& lay, char* ws, cudaStream_t s) {
     if (T == 0) return cudaSuccess;

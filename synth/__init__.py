@@ -134,6 +134,12 @@ WORKLOADS = {
                          description="DeepSeek-V3-shaped prefill layer, T=32768, Zipf(1.2) expert bias"),
     "kimi_64k": Workload("kimi_64k", 65536, 7168, 2048, 384, 8,
                          description="Kimi-K2-shaped prefill layer, T=65536, 384 experts"),
+    # profiling case: DeepSeek-V3 expert shapes and ~256 rows per expert (as
+    # at T=8192) with 32 experts, small enough for a full counter capture
+    "ds_prefill_probe": Workload("ds_prefill_probe", 1024, 7168, 2048, 32, 8,
+                                 description="DeepSeek-V3 expert shapes, 32 experts, T=1024 (profiling)"),
+    "ds_decode_probe": Workload("ds_decode_probe", 16, 7168, 2048, 32, 8,
+                                description="DeepSeek-V3 expert shapes, 32 experts, T=16 (profiling)"),
 }
 
 
