@@ -227,7 +227,7 @@ MOE_EXPORT moe_status moe_create(const moe_desc* d, const moe_weights* w, void* 
     else L->d.shared_inter = d->inter;
     L->wait_limit = kDefaultWaitLimitUs;
     auto cleanup = [&](moe_status st) {
-        cudaFree(L->w_gu); cudaFree(L->w_dn); cudaFree(L->s_gu); cudaFree(L->s_dn);
+        cudaFree(L->w_gu); cudaFree(L->w_dn); cudaFree(L->s_gu); cudaFree(L->s_dn); cudaFree(L->r_gu); cudaFree(L->r_dn);
         cudaFree(L->router_w); cudaFree(L->router_b); cudaFree(L->dev_status);
         delete L;
         return st;
@@ -243,6 +243,9 @@ MOE_EXPORT moe_status moe_create(const moe_desc* d, const moe_weights* w, void* 
     if ((e = cudaMalloc(&L->w_dn, dn)) != cudaSuccess) return cleanup(cuda_fail(e, "allocating down tiles"));
     if ((e = cudaMalloc(&L->s_gu, sgu)) != cudaSuccess) return cleanup(cuda_fail(e, "allocating scales"));
     if ((e = cudaMalloc(&L->s_dn, sdn)) != cudaSuccess) return cleanup(cuda_fail(e, "allocating scales"));
+    const size_t rgu = G * (I / moe::QB) * (H / moe::QB) * 16, rdn = G * ((H / moe::QB + 1) / 2) * (I / moe::QB) * 16;
+    if ((e = cudaMalloc(&L->r_gu, rgu)) != cudaSuccess) return cleanup(cuda_fail(e, "allocating scale records"));
+    if ((e = cudaMalloc(&L->r_dn, rdn)) != cudaSuccess) return cleanup(cuda_fail(e, "allocating scale records"));
     if ((e = cudaMalloc(&L->router_w, E * H * 4)) != cudaSuccess) return cleanup(cuda_fail(e, "allocating router"));
     if ((e = cudaMalloc(&L->router_b, E * 4)) != cudaSuccess) return cleanup(cuda_fail(e, "allocating bias"));
     if ((e = cudaMalloc(&L->dev_status, 4)) != cudaSuccess) return cleanup(cuda_fail(e, "allocating status"));
@@ -253,6 +256,7 @@ MOE_EXPORT moe_status moe_create(const moe_desc* d, const moe_weights* w, void* 
                        : cudaMemsetAsync(L->router_b, 0, E * 4, s);
     if (e != cudaSuccess) return cleanup(cuda_fail(e, "copying router bias"));
     if ((e = moe::launch_repack(L, w, s)) != cudaSuccess) return cleanup(cuda_fail(e, "weight repack"));
+    if ((e = moe::launch_tc_scale_records(L, s)) != cudaSuccess) return cleanup(cuda_fail(e, "scale records"));
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cleanup(cuda_fail(e, "moe_create synchronise"));
     *out = L;
     return MOE_OK;
@@ -263,7 +267,7 @@ MOE_EXPORT moe_status moe_destroy(moe_layer* L) {
     cudaError_t e = cudaDeviceSynchronize();
     if (L->profile)
         for (cudaEvent_t ev : L->ev) cudaEventDestroy(ev);
-    cudaFree(L->w_gu); cudaFree(L->w_dn); cudaFree(L->s_gu); cudaFree(L->s_dn);
+    cudaFree(L->w_gu); cudaFree(L->w_dn); cudaFree(L->s_gu); cudaFree(L->s_dn); cudaFree(L->r_gu); cudaFree(L->r_dn);
     cudaFree(L->router_w); cudaFree(L->router_b); cudaFree(L->dev_status);
     delete L;
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_destroy synchronise");

@@ -81,7 +81,6 @@ __device__ __forceinline__ Unit decode_unit(const GroupTable* gt, int u, int MT)
     return r;
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
 
 template <bool GU>
 __global__ void __launch_bounds__(NTHREADS, 1) expert_gemm_kernel(ExpertArgs a) {
@@ -260,7 +259,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_gemm_kernel(ExpertArgs a) 
 #pragma unroll
                         for (int w2 = 0; w2 < CW; ++w2) am = fmaxf(am, amax_s[w2 * BN + col]);
                         const float sc = (am > 0.f) ? __fdiv_rn(am, 448.0f) : 1.0f;
-                        const uint16_t pq = f32x2_to_e4m3x2(__fdiv_rn(h[nt][j], sc), __fdiv_rn(h[nt][2 + j], sc));
+                        const float rs = __frcp_rn(sc);                  // h / s as h * (1/s), as in prefill
+                        const uint16_t pq = f32x2_to_e4m3x2(h[nt][j] * rs, h[nt][2 + j] * rs);
                         qst[col * 144 + r0] = (uint8_t)(pq & 0xFF);
                         qst[col * 144 + r0 + 8] = (uint8_t)(pq >> 8);
                         if (warp == 0 && g == 0 && col < un.valid)

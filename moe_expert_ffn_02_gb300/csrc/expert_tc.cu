@@ -16,8 +16,12 @@
 // article, Fig. 9-10: a 128-element block's partial sum is scaled once):
 // each TMEM lane is one token, so its activation scale s_x[token][kb] is a
 // per-thread scalar and the weight scales s_w[kb] are uniform; the epilogue
-// warps read each block's partial with tcgen05.ld and promote it with packed
-// fp32x2 FMAs into registers.  Gate/up then forms h = SiLU(g)*u and its
+// warps read each block's partial with tcgen05.ld and promote it with fp32
+// FMAs into registers (scalar FFMA on the loaded registers: packing them into
+// pairs for fma.rn.f32x2 costs more moves than it saves).  Both scales ride in the stage with the
+// operands (two more bulk copies), so the epilogue reads them from shared
+// memory; a stage is free again once the MMAs that read it have completed
+// and all epilogue warps have taken their scales.  Gate/up then forms h = SiLU(g)*u and its
 // 1x128 E4M3 codes (the activation and elementwise product between gate/up
 // and down, "CPU fine-grained parallelism" section of the same article);
 // down writes fp32 output rows.
@@ -44,12 +48,21 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr int STAGES = 4;
 constexpr int W_BYTES = 2 * TILE_BYTES;   // 256 weight rows
 constexpr int X_BYTES = BM * 128;         // 128 token rows
-constexpr int STAGE = W_BYTES + X_BYTES;
-constexpr int SMEM = STAGES * STAGE + 2 * 4 * 32 * 4 + 256;   // + amax exchange
+// Stage tail: the 128 tokens' activation scales of this k block (512 B)
+// and the weight-scale record (16 B), padded so the next stage's operand
+// images stay 1024-byte aligned.
+constexpr int S_BYTES = BM * 4;
+constexpr int R_BYTES = 16;
+constexpr int STAGE = W_BYTES + X_BYTES + 1024;
+// Group table copy (expert, first row, rows, first tile of each group):
+// units are decoded from shared memory, never by a chain of L2 loads.
+constexpr int GT_CAP = MAX_EXPERTS + 2;
+constexpr int GT_BYTES = 4 * GT_CAP * 4;
+constexpr int SMEM = STAGES * STAGE + 2 * 4 * 32 * 4 + GT_BYTES + 256;   // + amax exchange + group table
 
 struct Args {
     const uint8_t* w;         // tile images of all groups
-    const float* wscale;      // [group][m tile][k tile] (x2 gate/up)
+    const float* wrec;        // [group][weight block][k tile][4] weight-scale records
     const uint8_t* act;       // [K/128][rows_pad][128] swizzled E4M3
     const float* actsT;       // [K/128][rows_pad]
     int ld;                   // rows_pad
@@ -66,21 +79,30 @@ struct Unit {
     int expert, wb, row_begin, valid;
 };
 
+// Shared-memory copy of the group table's arrays.
+struct SGroups {
+    int* expert;
+    int* row0;
+    int* rows;
+    int* pair_start;
+    int n_groups;
+};
+
 // u -> (group, token tile, weight block) with the weight block fastest.
 // NB = weight blocks per group (I/128 for gate/up, ceil(H/256) for down).
-__device__ __forceinline__ Unit decode_unit(const GroupTable* gt, int u, int NB) {
+__device__ __forceinline__ Unit decode_unit(const SGroups& g, int u, int NB) {
     const int pair = u / NB;
     Unit r;
     r.wb = u - pair * NB;
-    int lo = 0, hi = gt->n_groups - 1;            // last group with pair_start <= pair
+    int lo = 0, hi = g.n_groups - 1;              // last group with pair_start <= pair
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (gt->pair_start[mid] <= pair) lo = mid; else hi = mid - 1;
+        if (g.pair_start[mid] <= pair) lo = mid; else hi = mid - 1;
     }
-    const int nt = pair - gt->pair_start[lo];
-    r.expert = gt->expert[lo];
-    r.row_begin = gt->row0[lo] + nt * BM;
-    r.valid = min(BM, gt->rows[lo] - nt * BM);
+    const int nt = pair - g.pair_start[lo];
+    r.expert = g.expert[lo];
+    r.row_begin = g.row0[lo] + nt * BM;
+    r.valid = min(BM, g.rows[lo] - nt * BM);
     return r;
 }
 
@@ -144,21 +166,6 @@ __device__ __forceinline__ void tmem_ld32u(uint32_t taddr, uint32_t (&r)[32]) {
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// Packed fp32 pairs: acc += p * c on two lanes with one fma.rn.f32x2, each
-// lane rounded exactly like fmaf.  Accumulators stay packed for a whole unit.
-__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
-    return r;
-}
-__device__ __forceinline__ void fma2(uint64_t& acc, uint64_t p, uint64_t c) {
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(p), "l"(c));
-}
-__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
 
 // ------------------------------------------------------------------ kernel
 template <bool GU>
@@ -167,6 +174,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
     float* amax_x = reinterpret_cast<float*>(smem + STAGES * STAGE);   // [2 halves][4 quarters][32 lanes]
+    int* gt_s = reinterpret_cast<int*>(smem + STAGES * STAGE + 2 * 4 * 32 * 4);
     __shared__ uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
@@ -177,9 +185,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
     const int NB = GU ? MT128 : (MT128 + 1) / 2;             // weight blocks per unit row
     const GroupTable* gt = a.gt;
     const int n_units = gt->n_pairs * NB;
+    SGroups sg;
+    sg.n_groups = min(gt->n_groups, GT_CAP - 1);
+    sg.expert = gt_s;
+    sg.row0 = gt_s + GT_CAP;
+    sg.rows = gt_s + 2 * GT_CAP;
+    sg.pair_start = gt_s + 3 * GT_CAP;
+    for (int i = threadIdx.x; i < sg.n_groups; i += NTHREADS) {
+        sg.expert[i] = gt->expert[i];
+        sg.row0[i] = gt->row0[i];
+        sg.rows[i] = gt->rows[i];
+        sg.pair_start[i] = gt->pair_start[i];
+    }
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1 + EPI_WARPS); }
         for (int b = 0; b < 2; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], EPI_WARPS); }
         fence_mbar_init();
         abort_flag = 0;
@@ -199,7 +219,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
             uint32_t phase = 0, armed = 0, armed_par = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                const Unit un = decode_unit(gt, u, NB);
+                const Unit un = decode_unit(sg, u, NB);
                 // gate/up: the gate+up pair of inner tile wb (32 KB, contiguous per k block);
                 // down: tiles 2wb and 2wb+1 of the output rows (16 KB each, KT tiles apart)
                 const int t0 = GU ? un.wb : 2 * un.wb;
@@ -212,7 +232,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
                         break;
                     }
                     uint8_t* st = stages + stage * STAGE;
-                    mbar_arrive_expect_tx(&full[stage], wbytes + X_BYTES);
+                    mbar_arrive_expect_tx(&full[stage], wbytes + X_BYTES + S_BYTES + R_BYTES);
                     if (GU) {
                         bulk_g2s(st, wbase + (size_t)kb * W_BYTES, W_BYTES, &full[stage]);
                     } else {
@@ -221,6 +241,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
                             bulk_g2s(st + TILE_BYTES, wbase + ((size_t)KT + kb) * TILE_BYTES, TILE_BYTES, &full[stage]);
                     }
                     bulk_g2s(st + W_BYTES, a.act + act_offset(kb, un.row_begin, a.ld), X_BYTES, &full[stage]);
+                    bulk_g2s(st + W_BYTES + X_BYTES, a.actsT + (size_t)kb * a.ld + un.row_begin, S_BYTES, &full[stage]);
+                    bulk_g2s(st + W_BYTES + X_BYTES + S_BYTES, a.wrec + (((size_t)un.expert * NB + un.wb) * KT + kb) * 4,
+                             R_BYTES, &full[stage]);
                     armed |= 1u << stage;
                     armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -267,105 +290,87 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
         const int quarter = warp & 3;               // TMEM lanes this warp may read
         const int half = ew >> 2;                   // column half of the 256-column buffer
         const int r = quarter * 32 + lane;          // token row inside the tile
-        int buf = 0;
+        int buf = 0, stage = 0;
         uint32_t tphase = 0;
         bool dead = false;
         for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-            const Unit un = decode_unit(gt, u, NB);
+            const Unit un = decode_unit(sg, u, NB);
             const bool rv = r < un.valid;
             const size_t arow = (size_t)un.row_begin + r;
             const int t0 = GU ? un.wb : 2 * un.wb;
             const bool two = GU || (t0 + 1 < MT128);
-            // weight scales: gate/up j = 0 gate, 1 up; down: my half's tile (t0 + half)
-            const float* ws0 = GU ? a.wscale + ((size_t)(un.expert * MT128 + t0) * KT) * 2
-                                  : a.wscale + ((size_t)(un.expert * MT128 + t0 + ((half && two) ? 1 : 0)) * KT);
-            float wreg[2][2];                          // blocks lane and lane + 32
+            float acc[HALF];                          // 128 fp32 accumulators (my row, my columns)
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const int kb = lane + 32 * i;
-                    float v = 0.f;
-                    if (kb < KT && (GU || j == 0)) v = GU ? __ldg(ws0 + (size_t)kb * 2 + j) : __ldg(ws0 + kb);
-                    wreg[j][i] = v;
-                }
-            uint64_t acc[HALF / 2];                   // 128 fp32 accumulators, packed in pairs
-#pragma unroll
-            for (int c = 0; c < HALF / 2; ++c) acc[c] = 0ull;
-            constexpr int SXD = 4;                    // activation-scale prefetch distance (blocks)
-            float sxr[SXD];
-#pragma unroll
-            for (int d = 0; d < SXD; ++d) sxr[d] = (rv && d < KT) ? __ldg(a.actsT + (size_t)d * a.ld + arow) : 0.f;
-            for (int kb0 = 0; kb0 < KT; kb0 += SXD) {
-#pragma unroll
-                for (int d = 0; d < SXD; ++d) {
-                    const int kb = kb0 + d;
-                    if (kb >= KT) break;
-                    // per-thread combined scales for this block: s_w[j][kb] * s_x[token][kb]
-                    float cj[2];
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        float sw;
-                        if (KT <= 64) sw = __shfl_sync(0xFFFFFFFFu, kb < 32 ? wreg[j][0] : wreg[j][1], kb & 31);
-                        else sw = (GU || j == 0) ? (GU ? __ldg(ws0 + (size_t)kb * 2 + j) : __ldg(ws0 + kb)) : 0.f;
-                        cj[j] = sw * sxr[d];
-                    }
-                    if (kb + SXD < KT) sxr[d] = rv ? __ldg(a.actsT + (size_t)(kb + SXD) * a.ld + arow) : 0.f;
-                    if (!dead && !mbar_wait_bounded(&tfull[buf], tphase, a.wait_limit, a.status, abort)) dead = true;
-                    if (!dead) {
-                        tc_fence_after();
-                        const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN);
-                        // two TMEM round trips of 64 columns each
-#pragma unroll
-                        for (int ch = 0; ch < 2; ++ch) {
-                            uint32_t pv[2][32];
-                            if (GU) {
-                                // gate cols [64h + 32ch, +32) and up cols [128 + 64h + 32ch, +32)
-                                tmem_ld32u(tb + (uint32_t)(64 * half + 32 * ch), pv[0]);
-                                tmem_ld32u(tb + (uint32_t)(128 + 64 * half + 32 * ch), pv[1]);
-                            } else {
-                                tmem_ld32u(tb + (uint32_t)(128 * half + 64 * ch), pv[0]);
-                                tmem_ld32u(tb + (uint32_t)(128 * half + 64 * ch + 32), pv[1]);
-                            }
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int j = 0; j < 2; ++j) {
-                                // gate/up: j = 0 gate, 1 up (scales cj[0], cj[1]); down: one scale per half
-                                const float c = GU ? cj[j] : cj[0];
-                                const uint64_t cc = pack2(__float_as_uint(c), __float_as_uint(c));
-                                const int base = GU ? (j * 32 + ch * 16) : (ch * 32 + j * 16);
-#pragma unroll
-                                for (int q = 0; q < 16; ++q)
-                                    fma2(acc[base + q], pack2(pv[j][2 * q], pv[j][2 * q + 1]), cc);
-                            }
-                        }
-                        tc_fence_before();
-                    }
+            for (int c = 0; c < HALF; ++c) acc[c] = 0.f;
+            for (int kb = 0; kb < KT; ++kb) {
+                // No wait on full[stage] here: the MMA thread waited for the stage's copies
+                // (scales included) to land before issuing the MMAs whose completion
+                // signals tfull, so they have landed by the time tfull completes.
+                if (!dead && !mbar_wait_bounded(&tfull[buf], tphase, a.wait_limit, a.status, abort)) dead = true;
+                if (!dead) {
+                    tc_fence_after();
+                    // this block's scales from the stage tail: s_x of my token, the record's weight scales
+                    const uint8_t* tail = stages + stage * STAGE + W_BYTES + X_BYTES;
+                    const float sx = reinterpret_cast<const float*>(tail)[r];
+                    const float2 sw = *reinterpret_cast<const float2*>(tail + S_BYTES);
+                    const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN);
+                    // Four 32-column chunks, software-pipelined: the next chunk's tcgen05.ld is
+                    // in flight while this chunk's FMAs issue, and the wait that follows them
+                    // covers that load.  Gate/up chunk i: gate (i even) or up (i odd) columns
+                    // [64h + 32(i/2), +32) of its 128-column tile, accumulators
+                    // 32(i%2) + 16(i/2); down: columns [128h + 32i, +32), accumulators 16i.
+                    auto col_of = [&](int i) -> uint32_t {
+                        return GU ? (uint32_t)((i & 1) * 128 + 64 * half + 32 * (i >> 1)) : (uint32_t)(128 * half + 32 * i);
+                    };
+                    uint32_t pa[32], pb[32];
+                    tmem_ld32u(tb + col_of(0), pa);
+                    // combined scales s_w * s_x (gate/up: c0 gate, c1 up; down: my half's tile)
+                    const float c0 = (GU || half == 0) ? sw.x * sx : sw.y * sx;
+                    const float c1 = sw.y * sx;
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&tempty[buf]);
-                    if (++buf == 2) { buf = 0; tphase ^= 1u; }
+                    if (lane == 0) mbar_arrive(&empty[stage]);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t(&cur)[32] = (i & 1) ? pb : pa;
+                        uint32_t(&nxt)[32] = (i & 1) ? pa : pb;
+                        if (i < 3) tmem_ld32u(tb + col_of(i + 1), nxt);
+                        const float c = (GU && (i & 1)) ? c1 : c0;
+                        const int base = GU ? ((i & 1) * 32 + (i >> 1) * 16) : 16 * i;
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) acc[2 * base + q] = fmaf(__uint_as_float(cur[q]), c, acc[2 * base + q]);
+                        if (i < 3) tmem_wait_ld();
+                    }
+                    tc_fence_before();
+                } else {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[stage]);
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[buf]);
+                if (++buf == 2) { buf = 0; tphase ^= 1u; }
+                if (++stage == STAGES) stage = 0;
             }
 
             if (GU) {
                 // ------------------------------------------ SiLU(g)*u, 1x128 E4M3 quantisation of h
-                // this thread: features [64h, 64h+64) of the 128-feature tile; gate in acc[0..31],
-                // up in acc[32..63]
+                // this thread: features [64h, 64h+64) of the 128-feature tile; gate in acc[0..63],
+                // up in acc[64..127]
                 float h[64];
                 float amax = 0.f;
 #pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    float g0, g1, u0, u1;
-                    unpack2(acc[q], g0, g1);
-                    unpack2(acc[32 + q], u0, u1);
-                    h[2 * q] = silu_mul(g0, u0);
-                    h[2 * q + 1] = silu_mul(g1, u1);
-                    amax = fmaxf(amax, fmaxf(fabsf(h[2 * q]), fabsf(h[2 * q + 1])));
+                for (int e = 0; e < 64; ++e) {
+                    h[e] = silu_mul(acc[e], acc[64 + e]);
+                    amax = fmaxf(amax, fabsf(h[e]));
                 }
                 amax_x[(half * 4 + quarter) * 32 + lane] = amax;
                 named_bar_sync(1, EPI_WARPS * 32);
                 const float mx = fmaxf(amax, amax_x[((1 - half) * 4 + quarter) * 32 + lane]);
                 const float sc = (mx > 0.f) ? __fdiv_rn(mx, 448.0f) : 1.0f;
+                // h / s as h * (1/s): within one ulp of the rounded quotient, far inside
+                // the E4M3 code spacing, so a code can differ only for h at a rounding
+                // midpoint of the code grid
+                const float rs = __frcp_rn(sc);
                 if (rv) {
                     uint8_t* dst = a.hq + act_offset(un.wb, un.row_begin + r, a.ld);
 #pragma unroll
@@ -374,8 +379,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
                             const int e = c4 * 16 + k * 4;
-                            w4[k] = pack4_e4m3(__fdiv_rn(h[e], sc), __fdiv_rn(h[e + 1], sc), __fdiv_rn(h[e + 2], sc),
-                                               __fdiv_rn(h[e + 3], sc));
+                            w4[k] = pack4_e4m3(h[e] * rs, h[e + 1] * rs, h[e + 2] * rs, h[e + 3] * rs);
                         }
                         const int chunk = (half * 4 + c4) ^ (r & 7);     // row_begin is a multiple of 8
                         *reinterpret_cast<uint4*>(dst + chunk * 16) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
@@ -388,12 +392,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
                 if (rv && (half == 0 || two)) {
                     float* dst = a.out + arow * a.M + (size_t)un.wb * BN + half * HALF;
 #pragma unroll
-                    for (int q = 0; q < HALF / 4; ++q) {
-                        float v0, v1, v2, v3;
-                        unpack2(acc[2 * q], v0, v1);
-                        unpack2(acc[2 * q + 1], v2, v3);
-                        *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(v0, v1, v2, v3);
-                    }
+                    for (int q = 0; q < HALF / 4; ++q)
+                        *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
                 }
             }
         }
@@ -423,12 +423,12 @@ static cudaError_t launch(const moe_layer* L, const WsLayout& lay, char* ws, cud
     a.shT = reinterpret_cast<float*>(ws + lay.shT);
     a.out = reinterpret_cast<float*>(ws + lay.o);
     if (GU) {
-        a.w = L->w_gu; a.wscale = L->s_gu;
+        a.w = L->w_gu; a.wrec = L->r_gu;
         a.act = reinterpret_cast<const uint8_t*>(ws + lay.xp);
         a.actsT = reinterpret_cast<const float*>(ws + lay.sxT);
         a.K = H; a.M = I;
     } else {
-        a.w = L->w_dn; a.wscale = L->s_dn;
+        a.w = L->w_dn; a.wrec = L->r_dn;
         a.act = reinterpret_cast<const uint8_t*>(ws + lay.hq);
         a.actsT = reinterpret_cast<const float*>(ws + lay.shT);
         a.K = I; a.M = H;
@@ -437,9 +437,39 @@ static cudaError_t launch(const moe_layer* L, const WsLayout& lay, char* ws, cud
     return cudaGetLastError();
 }
 
+// Weight-scale records, built once at load time from the repacked scales:
+// one 16-byte record per (group, weight block, k block), so each stage
+// fetches its weight scales with one bulk copy.
+__global__ void scale_records_kernel(const float* __restrict__ s_gu, const float* __restrict__ s_dn, int G, int IT,
+                                     int HT, float4* __restrict__ r_gu, float4* __restrict__ r_dn) {
+    const int NBD = (HT + 1) / 2;
+    const size_t n_gu = (size_t)G * IT * HT, n_dn = (size_t)G * NBD * IT;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n_gu + n_dn; i += (size_t)gridDim.x * blockDim.x) {
+        if (i < n_gu) {
+            r_gu[i] = make_float4(s_gu[2 * i], s_gu[2 * i + 1], 0.f, 0.f);
+        } else {
+            const size_t j = i - n_gu;                 // (g, b, kb), kb fastest
+            const int kb = (int)(j % IT);
+            const int b = (int)((j / IT) % NBD);
+            const size_t g = j / ((size_t)IT * NBD);
+            const float lo = s_dn[(g * HT + 2 * b) * IT + kb];
+            const float hi = (2 * b + 1 < HT) ? s_dn[(g * HT + 2 * b + 1) * IT + kb] : 0.f;
+            r_dn[j] = make_float4(lo, hi, 0.f, 0.f);
+        }
+    }
+}
+
 }  // namespace tc
 
 int tc_tile_n() { return tc::BM; }
+
+cudaError_t launch_tc_scale_records(const moe_layer* L, cudaStream_t s) {
+    const int G = L->n_groups_max, IT = L->d.inter / QB, HT = L->d.hidden / QB;
+    tc::scale_records_kernel<<<4 * L->num_sms, 256, 0, s>>>(L->s_gu, L->s_dn, G, IT, HT,
+                                                           reinterpret_cast<float4*>(L->r_gu),
+                                                           reinterpret_cast<float4*>(L->r_dn));
+    return cudaGetLastError();
+}
 
 cudaError_t launch_expert_tc_gate_up(const moe_layer* L, int T, const WsLayout& lay, char* ws, cudaStream_t s) {
     if (T == 0) return cudaSuccess;

@@ -92,6 +92,8 @@ struct moe_layer {
     uint8_t* w_dn;         // [G][H/128][I/128][16 KB]    down tile images
     float* s_gu;           // [G][I/128][H/128][2]
     float* s_dn;           // [G][H/128][I/128]
+    float* r_gu;           // [G][I/128][H/128][4]: {gate, up, 0, 0} per k block (16-byte records)
+    float* r_dn;           // [G][ceil(H/256)][I/128][4]: {s(2b), s(2b+1) or 0, 0, 0} per k block
     float* router_w;       // [E][H]
     float* router_b;       // [E] (zeros when no bias)
     uint32_t* dev_status;  // device status word
@@ -225,6 +227,13 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float 
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
+// SiLU(g) * u, shared by the prefill and decode epilogues so both paths form
+// the same h.  Fast divide: h only needs a few-ulp accuracy before its 1x128
+// quantisation; for g < -87, exp(-g) = inf and the quotient is -0.  The
+// quantisation that follows takes h / s as h * (1/s), within one ulp of the
+// rounded quotient and far inside the E4M3 code spacing.
+__device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
+
 }  // namespace moe
 
 // Launchers (defined in the .cu files, called from api.cu).
@@ -246,6 +255,7 @@ cudaError_t launch_h_gather(const moe_layer* L, int T, const WsLayout& lay, char
                             cudaStream_t s);
 int tc_tile_n();
 cudaError_t launch_expert_tc_gate_up(const moe_layer* L, int T, const WsLayout& lay, char* ws, cudaStream_t s);
+cudaError_t launch_tc_scale_records(const moe_layer* L, cudaStream_t s);
 cudaError_t launch_expert_tc_down(const moe_layer* L, int T, const WsLayout& lay, char* ws, cudaStream_t s);
 cudaError_t launch_combine(const moe_layer* L, int T, const WsLayout& lay, char* ws, uint16_t* y, cudaStream_t s);
 cudaError_t launch_timeout_probe(const moe_layer* L, cudaStream_t s);

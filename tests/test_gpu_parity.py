@@ -144,10 +144,10 @@ def test_host_entry_matches_device_entry(h):
     wl = small_wl(16, 4, H=384, I=256, T=50)
     inp = synth.make_inputs(wl, seed=11)
     layer = h.make_layer(wl, inp)
-    y_dev, _ = h.run_forward(layer, inp["x"], 1, want_dbg=False)
     xh = torch.from_numpy(inp["x"].view(np.int16)).pin_memory()
     yh = torch.empty_like(xh).pin_memory()
     for mode in (1, 2):
+        y_dev, _ = h.run_forward(layer, inp["x"], mode, want_dbg=False)
         ws, nb = layer.workspace(wl.T, mode)
         moe.moe_forward_host(layer.handle, mode, xh.data_ptr(), wl.T, yh.data_ptr(), ws, nb, layer.stream)
         assert np.array_equal(yh.numpy().view(np.uint16), y_dev)
