@@ -11,7 +11,9 @@
 // of the CPU-GPU hybrid inference article (xingyun.xin, Fig. 9-10): the
 // products inside one 128-block are accumulated first (by the tensor core),
 // then the block is scaled once, here by s_w[block] * s_a[row][block], and
-// added to the fp32 accumulator.
+// added to the fp32 accumulator.  Both scales travel in the stage with the
+// operands (two more bulk copies), so the consumers never wait on a global
+// load inside the K loop.
 //
 // Gate/up kernel: both projections of the same 128 rows of the expert's
 // inner dimension share the activation fragments; the epilogue forms
@@ -36,19 +38,26 @@ constexpr int CW = 8;                   // consumer warps (16 output rows each)
 constexpr int NTHREADS = (CW + 1) * 32; // + producer warp
 constexpr int XSTRIDE = 128;            // activation row in shared memory (swizzled)
 
+// Stage tail: the tile rows' activation scales of this k block (BN floats)
+// and the 16-byte weight-scale record, brought by the producer with the
+// operands; padded so the next stage's weight tiles stay 1024-byte aligned.
+constexpr int S_BYTES = BN * 4;
+constexpr int R_BYTES = 16;
+constexpr int TAIL = 1024;
+
 template <bool GU>
 struct Cfg {
     static constexpr int W_BYTES = GU ? 2 * TILE_BYTES : TILE_BYTES;
     static constexpr int X_BYTES = BN * XSTRIDE;
-    static constexpr int STAGE = W_BYTES + X_BYTES;
+    static constexpr int STAGE = W_BYTES + X_BYTES + TAIL;
     static constexpr int STAGES = GU ? 4 : 6;
     static constexpr int EPI = GU ? (BN * 144 + CW * BN * 4) : (BN * 132 * 4);
-    static constexpr int SMEM = STAGES * STAGE + EPI + 2 * STAGES * 8 + 128;
+    static constexpr int SMEM = STAGES * STAGE + EPI + GT_SMEM_BYTES + 2 * STAGES * 8 + 128;
 };
 
 struct ExpertArgs {
     const uint8_t* w;         // tile images of all groups
-    const float* wscale;      // per (group, m tile, k tile) [x2 for gate/up]
+    const float* wrec;        // weight-scale records, [group][m tile (down: pair of m tiles)][k tile][4]
     const uint8_t* act;       // activations [K/128][rows_pad][128] (E4M3, swizzled)
     const float* actsT;       // activation scales [K/128][ld]
     int ld;                   // rows_pad of the permuted buffers
@@ -65,19 +74,11 @@ struct Unit {
     int expert, mb, row_begin, valid;
 };
 
-__device__ __forceinline__ Unit decode_unit(const GroupTable* gt, int u, int MT) {
+__device__ __forceinline__ Unit decode_unit(const SGroups& g, int u, int MT) {
     const int pair = u / MT;
     Unit r;
     r.mb = u - pair * MT;
-    int lo = 0, hi = gt->n_groups - 1;           // last group with pair_start <= pair
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (gt->pair_start[mid] <= pair) lo = mid; else hi = mid - 1;
-    }
-    const int nt = pair - gt->pair_start[lo];
-    r.expert = gt->expert[lo];
-    r.row_begin = gt->row0[lo] + nt * BN;
-    r.valid = min(BN, gt->rows[lo] - nt * BN);
+    decode_pair(g, pair, BN, r.expert, r.row_begin, r.valid);
     return r;
 }
 
@@ -89,7 +90,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_gemm_kernel(ExpertArgs a) 
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
     uint8_t* epi = smem + C::STAGES * C::STAGE;
-    uint64_t* full = reinterpret_cast<uint64_t*>(epi + C::EPI);
+    int* gt_s = reinterpret_cast<int*>(epi + C::EPI);
+    uint64_t* full = reinterpret_cast<uint64_t*>(epi + C::EPI + GT_SMEM_BYTES);
     uint64_t* empty = full + C::STAGES;
     __shared__ int abort_flag;
 
@@ -97,6 +99,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_gemm_kernel(ExpertArgs a) 
     const int MT = a.M / QB, KT = a.K / QB;
     const GroupTable* gt = a.gt;
     const int n_units = gt->n_pairs * MT;
+    const SGroups sg = load_groups(gt, gt_s, threadIdx.x, NTHREADS);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -116,16 +119,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_gemm_kernel(ExpertArgs a) 
         uint32_t armed = 0, armed_par = 0;       // per stage: armed at least once / parity of last arm
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-            const Unit un = decode_unit(gt, u, MT);
+            const Unit un = decode_unit(sg, u, MT);
             const uint8_t* wbase = a.w + ((size_t)(un.expert * MT + un.mb) * KT) * C::W_BYTES;
             for (int kb = 0; kb < KT; ++kb) {
                 if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, a.wait_limit, a.status, abort)) { ok = false; break; }
                 uint8_t* st = stages + stage * C::STAGE;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&full[stage], C::W_BYTES + un.valid * QB);
+                    mbar_arrive_expect_tx(&full[stage], C::W_BYTES + un.valid * QB + S_BYTES + R_BYTES);
                     bulk_g2s(st, wbase + (size_t)kb * C::W_BYTES, C::W_BYTES, &full[stage]);
                     bulk_g2s(st + C::W_BYTES, a.act + act_offset(kb, un.row_begin, a.ld), un.valid * QB,
                              &full[stage]);
+                    uint8_t* tail = st + C::W_BYTES + C::X_BYTES;
+                    bulk_g2s(tail, a.actsT + (size_t)kb * a.ld + un.row_begin, S_BYTES, &full[stage]);
+                    const size_t rec = GU ? ((size_t)un.expert * MT + un.mb) * KT + kb
+                                          : ((size_t)un.expert * ((MT + 1) / 2) + (un.mb >> 1)) * KT + kb;
+                    bulk_g2s(tail + S_BYTES, a.wrec + rec * 4, R_BYTES, &full[stage]);
                 }
                 __syncwarp();
                 armed |= 1u << stage;
@@ -148,9 +156,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_gemm_kernel(ExpertArgs a) 
     bool dead = false;    // a wait gave up: skip the math, keep the barriers
 
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const Unit un = decode_unit(gt, u, MT);
+        const Unit un = decode_unit(sg, u, MT);
         const int nt_active = (un.valid + 7) >> 3;
-        const float* wsc = a.wscale + ((size_t)(un.expert * MT + un.mb) * KT) * (GU ? 2 : 1);
         float accg[BN / 8][4], accu[BN / 8][4];
 #pragma unroll
         for (int nt = 0; nt < BN / 8; ++nt)
@@ -158,24 +165,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_gemm_kernel(ExpertArgs a) 
             for (int i = 0; i < 4; ++i) { accg[nt][i] = 0.f; accu[nt][i] = 0.f; }
 
         for (int kb = 0; kb < KT; ++kb) {
-            // activation scales of this lane's columns for block kb
-            float sa[BN / 8][2];
-#pragma unroll
-            for (int nt = 0; nt < BN / 8; ++nt)
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int col = nt * 8 + 2 * q + j;
-                    sa[nt][j] = (col < un.valid) ? __ldg(a.actsT + (size_t)kb * a.ld + un.row_begin + col) : 0.f;
-                }
-            const float swg = __ldg(wsc + (size_t)kb * (GU ? 2 : 1));
-            const float swu = GU ? __ldg(wsc + (size_t)kb * 2 + 1) : 0.f;
-
             if (!dead && !mbar_wait_bounded(&full[stage], phase, a.wait_limit, a.status, abort)) dead = true;
             if (dead) {
                 if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
                 continue;
             }
             const uint8_t* st = stages + stage * C::STAGE;
+            // scales from the stage tail: s_x of this lane's columns, the weight-scale record
+            // (gate/up: {gate, up}; down: {tile 2b, tile 2b+1} of the pair holding this m tile)
+            const float* tail = reinterpret_cast<const float*>(st + C::W_BYTES + C::X_BYTES);
+            const float2 rec = *reinterpret_cast<const float2*>(tail + BN);
+            const float swg = GU ? rec.x : ((un.mb & 1) ? rec.y : rec.x);
+            const float swu = rec.y;
+            float sa[BN / 8][2];
+#pragma unroll
+            for (int nt = 0; nt < BN / 8; ++nt) {
+                const float2 v = *reinterpret_cast<const float2*>(tail + nt * 8 + 2 * q);
+                sa[nt][0] = v.x;
+                sa[nt][1] = v.y;
+            }
             const uint8_t* X = st + C::W_BYTES;
             const uint4 ag0 = lds128(st + r0 * 128 + c0), ag1 = lds128(st + r0 * 128 + c1);
             const uint4 ag8 = lds128(st + (r0 + 8) * 128 + c0), ag9 = lds128(st + (r0 + 8) * 128 + c1);
@@ -321,12 +329,12 @@ static cudaError_t launch_expert(const moe_layer* L, const WsLayout& lay, char* 
     a.shT = reinterpret_cast<float*>(ws + lay.shT);
     a.out = reinterpret_cast<float*>(ws + lay.o);
     if (GU) {
-        a.w = L->w_gu; a.wscale = L->s_gu;
+        a.w = L->w_gu; a.wrec = L->r_gu;
         a.act = reinterpret_cast<const uint8_t*>(ws + lay.xp);
         a.actsT = reinterpret_cast<const float*>(ws + lay.sxT);
         a.K = H; a.M = I;
     } else {
-        a.w = L->w_dn; a.wscale = L->s_dn;
+        a.w = L->w_dn; a.wrec = L->r_dn;
         a.act = reinterpret_cast<const uint8_t*>(ws + lay.hq);
         a.actsT = reinterpret_cast<const float*>(ws + lay.shT);
         a.K = I; a.M = H;

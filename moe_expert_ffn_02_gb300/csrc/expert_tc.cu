@@ -54,11 +54,8 @@ constexpr int X_BYTES = BM * 128;         // 128 token rows
 constexpr int S_BYTES = BM * 4;
 constexpr int R_BYTES = 16;
 constexpr int STAGE = W_BYTES + X_BYTES + 1024;
-// Group table copy (expert, first row, rows, first tile of each group):
-// units are decoded from shared memory, never by a chain of L2 loads.
-constexpr int GT_CAP = MAX_EXPERTS + 2;
-constexpr int GT_BYTES = 4 * GT_CAP * 4;
-constexpr int SMEM = STAGES * STAGE + 2 * 4 * 32 * 4 + GT_BYTES + 256;   // + amax exchange + group table
+// + amax exchange + the group table copy (units are decoded from shared memory)
+constexpr int SMEM = STAGES * STAGE + 2 * 4 * 32 * 4 + GT_SMEM_BYTES + 256;
 
 struct Args {
     const uint8_t* w;         // tile images of all groups
@@ -79,30 +76,13 @@ struct Unit {
     int expert, wb, row_begin, valid;
 };
 
-// Shared-memory copy of the group table's arrays.
-struct SGroups {
-    int* expert;
-    int* row0;
-    int* rows;
-    int* pair_start;
-    int n_groups;
-};
-
 // u -> (group, token tile, weight block) with the weight block fastest.
 // NB = weight blocks per group (I/128 for gate/up, ceil(H/256) for down).
 __device__ __forceinline__ Unit decode_unit(const SGroups& g, int u, int NB) {
     const int pair = u / NB;
     Unit r;
     r.wb = u - pair * NB;
-    int lo = 0, hi = g.n_groups - 1;              // last group with pair_start <= pair
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (g.pair_start[mid] <= pair) lo = mid; else hi = mid - 1;
-    }
-    const int nt = pair - g.pair_start[lo];
-    r.expert = g.expert[lo];
-    r.row_begin = g.row0[lo] + nt * BM;
-    r.valid = min(BM, g.rows[lo] - nt * BM);
+    decode_pair(g, pair, BM, r.expert, r.row_begin, r.valid);
     return r;
 }
 
@@ -185,18 +165,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
     const int NB = GU ? MT128 : (MT128 + 1) / 2;             // weight blocks per unit row
     const GroupTable* gt = a.gt;
     const int n_units = gt->n_pairs * NB;
-    SGroups sg;
-    sg.n_groups = min(gt->n_groups, GT_CAP - 1);
-    sg.expert = gt_s;
-    sg.row0 = gt_s + GT_CAP;
-    sg.rows = gt_s + 2 * GT_CAP;
-    sg.pair_start = gt_s + 3 * GT_CAP;
-    for (int i = threadIdx.x; i < sg.n_groups; i += NTHREADS) {
-        sg.expert[i] = gt->expert[i];
-        sg.row0[i] = gt->row0[i];
-        sg.rows[i] = gt->rows[i];
-        sg.pair_start[i] = gt->pair_start[i];
-    }
+    const SGroups sg = load_groups(gt, gt_s, threadIdx.x, NTHREADS);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1 + EPI_WARPS); }

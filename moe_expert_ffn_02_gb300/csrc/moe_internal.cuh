@@ -57,6 +57,52 @@ struct GroupTable {
     int32_t pair_start[MAX_EXPERTS + 2];
 };
 
+// Shared-memory copy of a GroupTable's per-group arrays, so the expert GEMMs
+// decode their units without chains of dependent L2 loads.  GT_SMEM_BYTES
+// of dynamic shared memory hold it; load_groups is called by every thread of
+// the CTA before its first __syncthreads.
+constexpr int GT_CAP = MAX_EXPERTS + 2;
+constexpr int GT_SMEM_BYTES = 4 * GT_CAP * 4;
+
+struct SGroups {
+    int* expert;
+    int* row0;
+    int* rows;
+    int* pair_start;
+    int n_groups;
+};
+
+__device__ __forceinline__ SGroups load_groups(const GroupTable* gt, int* smem, int tid, int nthreads) {
+    SGroups g;
+    g.n_groups = min(gt->n_groups, GT_CAP - 1);
+    g.expert = smem;
+    g.row0 = smem + GT_CAP;
+    g.rows = smem + 2 * GT_CAP;
+    g.pair_start = smem + 3 * GT_CAP;
+    for (int i = tid; i < g.n_groups; i += nthreads) {
+        g.expert[i] = gt->expert[i];
+        g.row0[i] = gt->row0[i];
+        g.rows[i] = gt->rows[i];
+        g.pair_start[i] = gt->pair_start[i];
+    }
+    return g;
+}
+
+// Tile `pair` (a group's row tiles numbered consecutively over all groups)
+// -> its group's expert, the tile's first internal row and its row count.
+__device__ __forceinline__ void decode_pair(const SGroups& g, int pair, int tile_rows, int& expert, int& row_begin,
+                                            int& valid) {
+    int lo = 0, hi = g.n_groups - 1;              // last group with pair_start <= pair
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (g.pair_start[mid] <= pair) lo = mid; else hi = mid - 1;
+    }
+    const int nt = pair - g.pair_start[lo];
+    expert = g.expert[lo];
+    row_begin = g.row0[lo] + nt * tile_rows;
+    valid = min(tile_rows, g.rows[lo] - nt * tile_rows);
+}
+
 // Workspace carve-up for one call (all offsets 256-byte aligned).
 struct WsLayout {
     size_t logit_part;   // f32 [ksplit][T][E] router partial sums
