@@ -45,10 +45,12 @@ moe::WsLayout make_layout(const moe_layer* L, int T, int mode) {
     // internal rows: every routed group padded to ROW_ALIGN, then the shared group
     const size_t rows = R + (L->d.n_shared ? (size_t)T : 0) + (size_t)moe::ROW_ALIGN * (E + 1);
     l.rows_pad = (int)up(rows + moe::ROW_PAD, 64);
-    // router: T <= 64 -> one GEMV pass (ksplit 0); otherwise the tiled GEMM,
-    // split along H (a divisor of H/128) until the grid covers ~2 waves
-    if (T <= 64) {
-        l.ksplit = 0;
+    // router: T <= 64 -> the split GEMV; otherwise the tiled GEMM, split
+    // along H (a divisor of H/128) until the grid covers ~2 waves.  Either
+    // way ksplit partial sums, added in order by the top-k kernel.
+    l.gemv = T <= 64;
+    if (l.gemv) {
+        l.ksplit = moe::router_gemv_splits((int)H);
     } else {
         const int base = (int)((E + 63) / 64) * ((T + 63) / 64), hb = (int)(H / moe::QB);
         l.ksplit = 1;
@@ -58,7 +60,7 @@ moe::WsLayout make_layout(const moe_layer* L, int T, int mode) {
     l.n_chunks = (T + moe::CHUNK_TOK - 1) / moe::CHUNK_TOK;
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t o = off; off = up(off + bytes, 256); return o; };
-    l.logit_part = take((size_t)(l.ksplit > 0 ? l.ksplit : 1) * T * E * 4);
+    l.logit_part = take((size_t)l.ksplit * T * E * 4);
     l.logits = l.logit_part;
     l.ids = take(R * 4);
     l.w = take(R * 4);
@@ -118,8 +120,8 @@ moe_status run_route(moe_layer* L, const uint16_t* x, const float* logits_in, in
         MOE_CUDA(moe::launch_topk(L, logits_in, 1, false, T, nullptr, ids, w, s), "top-k");
     } else {
         float* part = reinterpret_cast<float*>(ws + lay.logit_part);
-        MOE_CUDA(moe::launch_router_logits(L, x, T, part, lay.ksplit, s), "router logits");
-        MOE_CUDA(moe::launch_topk(L, part, lay.ksplit > 0 ? lay.ksplit : 1, true, T, dbg ? dbg->logits : nullptr, ids,
+        MOE_CUDA(moe::launch_router_logits(L, x, T, part, lay.ksplit, lay.gemv, s), "router logits");
+        MOE_CUDA(moe::launch_topk(L, part, lay.ksplit, true, T, dbg ? dbg->logits : nullptr, ids,
                                   w, s),
                  "top-k");
     }

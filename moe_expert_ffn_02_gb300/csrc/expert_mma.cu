@@ -363,8 +363,8 @@ cudaError_t launch_expert_down(const moe_layer* L, int T, const WsLayout& lay, c
 // Combine ("weighted reduction" after the experts, SmallEP section of the
 // CPU-GPU hybrid inference article): per token, in this fixed order,
 //   y = O[shared row] + w_0 O[row_0] + ... + w_{k-1} O[row_{k-1}]
-// in fp32, rounded once to bf16.  One CTA per token, 4 channels per thread
-// per step.
+// in fp32, rounded once to bf16.  CTA (token, blockIdx.y) owns 1024
+// channels, 4 per thread.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ O, const int32_t* __restrict__ inv_int,
                                                       const float* __restrict__ w, const int32_t* __restrict__ offsets_pad,
@@ -379,7 +379,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     }
     __syncthreads();
     const size_t shrow = (size_t)offsets_pad[E] + t;
-    for (int c = threadIdx.x * 4; c < H; c += blockDim.x * 4) {
+    for (int c = (blockIdx.y * blockDim.x + threadIdx.x) * 4; c < H; c += gridDim.y * blockDim.x * 4) {
         float4 acc = n_shared ? *reinterpret_cast<const float4*>(O + shrow * H + c) : make_float4(0.f, 0.f, 0.f, 0.f);
         for (int j = 0; j < k; ++j) {
             const float4 o = *reinterpret_cast<const float4*>(O + (size_t)rows[j] * H + c);
@@ -400,7 +400,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 
 cudaError_t launch_combine(const moe_layer* L, int T, const WsLayout& lay, char* ws, uint16_t* y, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    combine_kernel<<<T, 256, 0, s>>>(reinterpret_cast<const float*>(ws + lay.o),
+    // CTA (token, blockIdx.y) owns channels [1024 blockIdx.y, +1024): one float4 per thread
+    const dim3 grid(T, (L->d.hidden + 1023) / 1024);
+    combine_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const float*>(ws + lay.o),
                                      reinterpret_cast<const int32_t*>(ws + lay.inv_int),
                                      reinterpret_cast<const float*>(ws + lay.w),
                                      reinterpret_cast<const int32_t*>(ws + lay.offsets_pad), T, L->d.hidden, L->d.top_k,

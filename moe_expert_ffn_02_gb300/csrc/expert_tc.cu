@@ -5,7 +5,8 @@
 // 128 per stage.  Gate/up: B = the expert's gate tile and up tile of the
 // same 128 inner features, which sit next to each other in the repacked
 // weights, so one M128 x N256 x K32 MMA covers both projections.  Down: B =
-// two consecutive 128-row tiles of the down weights (256 outputs).  Both
+// two consecutive 128-row tiles of the down weights (256 outputs), written as
+// fp32 expert-output rows.  Both
 // operands are 128-byte-swizzled K-major images that one bulk copy each
 // brings into shared memory.  One thread issues tcgen05.mma kind::f8f6f4
 // (E4M3 x E4M3, fp32 accumulate in tensor memory), 4 per stage, with
@@ -54,8 +55,16 @@ constexpr int X_BYTES = BM * 128;         // 128 token rows
 constexpr int S_BYTES = BM * 4;
 constexpr int R_BYTES = 16;
 constexpr int STAGE = W_BYTES + X_BYTES + 1024;
-// + amax exchange + the group table copy (units are decoded from shared memory)
-constexpr int SMEM = STAGES * STAGE + 2 * 4 * 32 * 4 + GT_SMEM_BYTES + 256;
+// + amax exchange + the group table copy (units are decoded from shared
+// memory; up to 385 groups, larger tables are read in place) + the down
+// epilogue's per-warp staging tiles (32 rows x 16 floats, rows 20 floats
+// apart so the row-wise writes are free of bank conflicts)
+constexpr int GT_SMEM_CAP = 386;
+constexpr int STG_STRIDE = 20;
+constexpr int STG_BYTES = EPI_WARPS * 32 * STG_STRIDE * 4;
+constexpr int SMEM = STAGES * STAGE + 2 * 4 * 32 * 4 + gt_smem_bytes(GT_SMEM_CAP) + STG_BYTES + 256;
+// dynamic (with 1024 bytes of alignment slack) + static (barriers, padded to 1024) <= 227 KB
+static_assert(SMEM + 1024 + 1024 <= 232448, "shared memory budget");
 
 struct Args {
     const uint8_t* w;         // tile images of all groups
@@ -67,7 +76,7 @@ struct Args {
     const GroupTable* gt;
     uint8_t* hq;              // gate/up output codes (same layout as act)
     float* shT;               // gate/up output scales
-    float* out;               // down: [rows_pad][M] fp32
+    float* out;               // down: [rows_pad][M] fp32 expert outputs
     uint32_t* status;
     uint32_t wait_limit;
 };
@@ -155,6 +164,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
     uint8_t* stages = smem;
     float* amax_x = reinterpret_cast<float*>(smem + STAGES * STAGE);   // [2 halves][4 quarters][32 lanes]
     int* gt_s = reinterpret_cast<int*>(smem + STAGES * STAGE + 2 * 4 * 32 * 4);
+    float* stg_all = reinterpret_cast<float*>(smem + STAGES * STAGE + 2 * 4 * 32 * 4 + gt_smem_bytes(GT_SMEM_CAP));
     __shared__ uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
@@ -165,7 +175,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
     const int NB = GU ? MT128 : (MT128 + 1) / 2;             // weight blocks per unit row
     const GroupTable* gt = a.gt;
     const int n_units = gt->n_pairs * NB;
-    const SGroups sg = load_groups(gt, gt_s, threadIdx.x, NTHREADS);
+    const SGroups sg = load_groups(gt, gt_s, threadIdx.x, NTHREADS, GT_SMEM_CAP);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1 + EPI_WARPS); }
@@ -265,7 +275,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
         for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
             const Unit un = decode_unit(sg, u, NB);
             const bool rv = r < un.valid;
-            const size_t arow = (size_t)un.row_begin + r;
             const int t0 = GU ? un.wb : 2 * un.wb;
             const bool two = GU || (t0 + 1 < MT128);
             float acc[HALF];                          // 128 fp32 accumulators (my row, my columns)
@@ -357,12 +366,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
                 }
                 named_bar_sync(1, EPI_WARPS * 32);
             } else {
-                // ------------------------------------------ fp32 expert output row: 128 features
-                if (rv && (half == 0 || two)) {
-                    float* dst = a.out + arow * a.M + (size_t)un.wb * BN + half * HALF;
+                // ------------------------------------------ fp32 expert output rows: 128 features
+                // Through the warp's staging tile, 16 columns at a time: each lane writes its
+                // row's 16 values, then lane l stores row 8p + l/4, columns 4(l%4)..+3, so one
+                // store instruction covers 8 rows x 64 contiguous bytes (full sectors) instead
+                // of 32 rows x 16 bytes.
+                float* stg = stg_all + (size_t)ew * 32 * STG_STRIDE;
+                const bool wr = half == 0 || two;
+                float* dst0 = a.out + (size_t)un.row_begin * a.M + (size_t)un.wb * BN + half * HALF + 4 * (lane & 3);
 #pragma unroll
-                    for (int q = 0; q < HALF / 4; ++q)
-                        *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+                for (int c0 = 0; c0 < HALF; c0 += 16) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        *reinterpret_cast<float4*>(stg + lane * STG_STRIDE + 4 * i) =
+                            make_float4(acc[c0 + 4 * i], acc[c0 + 4 * i + 1], acc[c0 + 4 * i + 2], acc[c0 + 4 * i + 3]);
+                    __syncwarp();
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) {
+                        const int rr = 8 * p + (lane >> 2);
+                        const float4 v = *reinterpret_cast<const float4*>(stg + rr * STG_STRIDE + 4 * (lane & 3));
+                        const int row = quarter * 32 + rr;
+                        if (wr && row < un.valid) *reinterpret_cast<float4*>(dst0 + (size_t)row * a.M + c0) = v;
+                    }
+                    __syncwarp();
                 }
             }
         }

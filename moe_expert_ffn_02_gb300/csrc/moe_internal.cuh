@@ -58,11 +58,13 @@ struct GroupTable {
 };
 
 // Shared-memory copy of a GroupTable's per-group arrays, so the expert GEMMs
-// decode their units without chains of dependent L2 loads.  GT_SMEM_BYTES
-// of dynamic shared memory hold it; load_groups is called by every thread of
-// the CTA before its first __syncthreads.
+// decode their units without chains of dependent L2 loads.  gt_smem_bytes(cap)
+// of dynamic shared memory hold up to cap - 1 groups; a table with more
+// groups is read in place from global memory.  load_groups is called by
+// every thread of the CTA before its first __syncthreads.
 constexpr int GT_CAP = MAX_EXPERTS + 2;
-constexpr int GT_SMEM_BYTES = 4 * GT_CAP * 4;
+__host__ __device__ constexpr int gt_smem_bytes(int cap) { return 4 * cap * 4; }
+constexpr int GT_SMEM_BYTES = gt_smem_bytes(GT_CAP);
 
 struct SGroups {
     int* expert;
@@ -72,13 +74,21 @@ struct SGroups {
     int n_groups;
 };
 
-__device__ __forceinline__ SGroups load_groups(const GroupTable* gt, int* smem, int tid, int nthreads) {
+__device__ __forceinline__ SGroups load_groups(const GroupTable* gt, int* smem, int tid, int nthreads,
+                                               int cap = GT_CAP) {
     SGroups g;
     g.n_groups = min(gt->n_groups, GT_CAP - 1);
+    if (g.n_groups > cap - 1) {                   // too many groups for the copy: use the table in place
+        g.expert = const_cast<int*>(gt->expert);
+        g.row0 = const_cast<int*>(gt->row0);
+        g.rows = const_cast<int*>(gt->rows);
+        g.pair_start = const_cast<int*>(gt->pair_start);
+        return g;
+    }
     g.expert = smem;
-    g.row0 = smem + GT_CAP;
-    g.rows = smem + 2 * GT_CAP;
-    g.pair_start = smem + 3 * GT_CAP;
+    g.row0 = smem + cap;
+    g.rows = smem + 2 * cap;
+    g.pair_start = smem + 3 * cap;
     for (int i = tid; i < g.n_groups; i += nthreads) {
         g.expert[i] = gt->expert[i];
         g.row0[i] = gt->row0[i];
@@ -123,6 +133,7 @@ struct WsLayout {
     size_t o;            // f32 [rows_pad][H]           expert outputs (unweighted)
     size_t total;
     int ksplit, n_chunks, rows_pad;
+    bool gemv;           // router logits by the split GEMV (decode batches)
 };
 
 constexpr int CHUNK_TOK = 64;         // tokens per permutation chunk (one warp)
@@ -285,7 +296,8 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(
 // Launchers (defined in the .cu files, called from api.cu).
 namespace moe {
 cudaError_t launch_repack(const moe_layer* L, const moe_weights* w, cudaStream_t s);
-cudaError_t launch_router_logits(const moe_layer* L, const uint16_t* x, int T, float* part, int ksplit,
+int router_gemv_splits(int H);
+cudaError_t launch_router_logits(const moe_layer* L, const uint16_t* x, int T, float* part, int ksplit, bool gemv,
                                  cudaStream_t s);
 cudaError_t launch_topk(const moe_layer* L, const float* part, int ksplit, bool add_bias, int T, float* logits_out,
                         int32_t* ids, float* w, cudaStream_t s);

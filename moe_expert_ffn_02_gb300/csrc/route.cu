@@ -115,76 +115,100 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __re
 
 // ---------------------------------------------------------------------------
 // Router logits for a decode batch (T <= 64): a GEMV over the fp32 router
-// weights, which dominate the bytes.  One CTA per pair of experts; warp w
-// owns channels [w*H/8, (w+1)*H/8); each lane accumulates its channels in
-// fp32 for every token, the lanes are combined by a shuffle tree and the
-// warps in a fixed order -- deterministic, and no partial sums leave the CTA.
+// weights, which dominate the bytes.  The channels are split into ksplit
+// slices (grid.y); a CTA stages its slice of x for up to GEMV_TC tokens in
+// shared memory and each of its 8 warps streams one expert's weight slice
+// with 16-byte loads, lane l taking channels 4l, 4l+128, ... in order.  The
+// lanes are combined by a fixed shuffle tree and the slice's partial sum
+// goes to part[slice][t][e]; the top-k kernel adds the slices in order, so
+// the result is deterministic.
 // ---------------------------------------------------------------------------
-constexpr int GEMV_E = 2, GEMV_WARPS = 8, GEMV_TMAX = 64;
+constexpr int GEMV_WARPS = 8, GEMV_TC = 16;
 
 __global__ void __launch_bounds__(GEMV_WARPS * 32) router_gemv_kernel(const uint16_t* __restrict__ x,
                                                                       const float* __restrict__ W, int T, int H,
-                                                                      int E, float* __restrict__ logits) {
-    __shared__ float red[GEMV_WARPS][GEMV_E][GEMV_TMAX];
+                                                                      int E, int slice, int tc,
+                                                                      float* __restrict__ part) {
+    extern __shared__ __align__(16) uint16_t xs[];              // [tc][slice]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e0 = blockIdx.x * GEMV_E;
-    const int span = H / GEMV_WARPS;                   // multiple of 16
-    const int h0 = warp * span;
-    for (int t0 = 0; t0 < T; t0 += 8) {                // 8 tokens at a time keeps the accumulators in registers
-        float acc[GEMV_E][8];
+    const int e = blockIdx.x * GEMV_WARPS + warp;
+    const int z = blockIdx.y;
+    const int h0 = z * slice;
+    const int n16 = slice / 8;                                   // 16-byte pieces per token row
+    for (int t0 = 0; t0 < T; t0 += tc) {
+        const int nt = min(tc, T - t0);
+        __syncthreads();
+        for (int i = threadIdx.x; i < nt * n16; i += blockDim.x) {
+            const int tt = i / n16, c = i - tt * n16;
+            *reinterpret_cast<uint4*>(xs + (size_t)tt * slice + c * 8) =
+                *reinterpret_cast<const uint4*>(x + (size_t)(t0 + tt) * H + h0 + c * 8);
+        }
+        __syncthreads();
+        if (e >= E) continue;
+        float acc[GEMV_TC];
 #pragma unroll
-        for (int j = 0; j < GEMV_E; ++j)
+        for (int u = 0; u < GEMV_TC; ++u) acc[u] = 0.f;
+        const float* wr = W + (size_t)e * H + h0;
+        // 8 weight loads of the lane in flight before the arithmetic that uses them
+        for (int c0 = lane * 4; c0 < slice; c0 += 8 * 128) {
+            float4 wv[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) acc[j][u] = 0.f;
-        for (int h = h0 + lane * 4; h < h0 + span; h += 128) {
-            float4 wv[GEMV_E];
+            for (int j = 0; j < 8; ++j)
+                wv[j] = (c0 + j * 128 < slice) ? __ldg(reinterpret_cast<const float4*>(wr + c0 + j * 128))
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int j = 0; j < GEMV_E; ++j)
-                wv[j] = (e0 + j < E) ? *reinterpret_cast<const float4*>(W + (size_t)(e0 + j) * H + h)
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < 8; ++j) {
+                const int c = c0 + j * 128;
+                if (c >= slice) break;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                if (t0 + u < T) {
-                    const uint2 raw = *reinterpret_cast<const uint2*>(x + (size_t)(t0 + u) * H + h);
-                    const float a0 = __uint_as_float(raw.x << 16), a1 = __uint_as_float(raw.x & 0xFFFF0000u);
-                    const float a2 = __uint_as_float(raw.y << 16), a3 = __uint_as_float(raw.y & 0xFFFF0000u);
-#pragma unroll
-                    for (int j = 0; j < GEMV_E; ++j) {
-                        float p = __fmul_rn(a0, wv[j].x);
-                        p = __fmaf_rn(a1, wv[j].y, p);
-                        p = __fmaf_rn(a2, wv[j].z, p);
-                        p = __fmaf_rn(a3, wv[j].w, p);
-                        acc[j][u] = __fadd_rn(acc[j][u], p);
+                for (int u = 0; u < GEMV_TC; ++u) {
+                    if (u < nt) {
+                        const uint2 raw = *reinterpret_cast<const uint2*>(xs + (size_t)u * slice + c);
+                        float p = __fmul_rn(__uint_as_float(raw.x << 16), wv[j].x);
+                        p = __fmaf_rn(__uint_as_float(raw.x & 0xFFFF0000u), wv[j].y, p);
+                        p = __fmaf_rn(__uint_as_float(raw.y << 16), wv[j].z, p);
+                        p = __fmaf_rn(__uint_as_float(raw.y & 0xFFFF0000u), wv[j].w, p);
+                        acc[u] = __fadd_rn(acc[u], p);
                     }
                 }
             }
         }
 #pragma unroll
-        for (int j = 0; j < GEMV_E; ++j)
+        for (int u = 0; u < GEMV_TC; ++u) {
+            float v = acc[u];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                float v = acc[j][u];
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
-                if (lane == 0 && t0 + u < T) red[warp][j][t0 + u] = v;
-            }
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < GEMV_E * T; i += blockDim.x) {
-        const int j = i / T, t = i - j * T;
-        if (e0 + j >= E) continue;
-        float v = red[0][j][t];
-        for (int w = 1; w < GEMV_WARPS; ++w) v = __fadd_rn(v, red[w][j][t]);
-        logits[(size_t)t * E + e0 + j] = v;
+            for (int off = 16; off > 0; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
+            if (lane == 0 && u < nt) part[((size_t)z * T + t0 + u) * E + e] = v;
+        }
     }
 }
 
-cudaError_t launch_router_logits(const moe_layer* L, const uint16_t* x, int T, float* part, int ksplit,
+// Slices for the GEMV: the largest divisor of H/128 that is at most 8.
+int router_gemv_splits(int H) {
+    const int hb = H / QB;
+    int d = 1;
+    for (int c = 1; c <= 8; ++c)
+        if (hb % c == 0) d = c;
+    return d;
+}
+
+cudaError_t launch_router_logits(const moe_layer* L, const uint16_t* x, int T, float* part, int ksplit, bool gemv,
                                  cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     const int H = L->d.hidden, E = L->d.n_experts;
-    if (ksplit == 0) {                                 // decode batch: GEMV, complete logits in part[0]
-        router_gemv_kernel<<<(E + GEMV_E - 1) / GEMV_E, GEMV_WARPS * 32, 0, s>>>(x, L->router_w, T, H, E, part);
+    if (gemv) {                                        // decode batch: split GEMV, ksplit partial sums
+        const int slice = H / ksplit;
+        const int tc = max(1, min(GEMV_TC, (160 * 1024) / (slice * 2)));
+        const size_t smem = (size_t)tc * slice * 2;
+        static bool attr = false;
+        if (!attr) {
+            cudaError_t e = cudaFuncSetAttribute(router_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 160 * 1024 + 4096);
+            if (e != cudaSuccess) return e;
+            attr = true;
+        }
+        dim3 grid((E + GEMV_WARPS - 1) / GEMV_WARPS, ksplit);
+        router_gemv_kernel<<<grid, GEMV_WARPS * 32, smem, s>>>(x, L->router_w, T, H, E, slice, tc, part);
         return cudaGetLastError();
     }
     dim3 grid((E + LE - 1) / LE, (T + LT - 1) / LT, ksplit);
@@ -242,16 +266,34 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     if (t >= T) return;
+    // logits: the ksplit partial sums added in split order, then the bias.  The
+    // partials are fetched ZB splits at a time for all PER experts of the lane
+    // before any addition, so the loads are in flight together.
+    constexpr int ZB = PER <= 8 ? 8 : (PER <= 16 ? 4 : 2);
     float v[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) v[i] = 0.f;
+    for (int z0 = 0; z0 < ksplit; z0 += ZB) {
+        float pv[PER][ZB];
+#pragma unroll
+        for (int i = 0; i < PER; ++i)
+#pragma unroll
+            for (int zz = 0; zz < ZB; ++zz) {
+                const int e = lane + 32 * i, z = z0 + zz;
+                pv[i][zz] = (e < E && z < ksplit) ? part[((size_t)z * T + t) * E + e] : 0.f;
+            }
+#pragma unroll
+        for (int i = 0; i < PER; ++i)
+#pragma unroll
+            for (int zz = 0; zz < ZB; ++zz)
+                if (z0 + zz < ksplit) v[i] = (z0 + zz == 0) ? pv[i][zz] : __fadd_rn(v[i], pv[i][zz]);
+    }
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
         const int e = lane + 32 * i;
         if (e < E) {
-            float acc = part[(size_t)t * E + e];
-            for (int z = 1; z < ksplit; ++z) acc = __fadd_rn(acc, part[((size_t)z * T + t) * E + e]);
-            if (bias) acc = __fadd_rn(acc, bias[e]);
-            v[i] = acc;
-            if (logits_out) logits_out[(size_t)t * E + e] = acc;
+            if (bias) v[i] = __fadd_rn(v[i], bias[e]);
+            if (logits_out) logits_out[(size_t)t * E + e] = v[i];
         } else {
             v[i] = -CUDART_INF_F;
         }
@@ -527,8 +569,9 @@ cudaError_t launch_permute(const moe_layer* L, const int32_t* ids, int T, const 
 // saturation.  Destination rows (internal, 8-aligned groups): inv_int[t][j]
 // for the routed groups and shared_row0 + t for the shared group; the codes
 // go to the swizzled K-block-major layout (see act_offset) and the scales
-// to sxT[g][row], so one tile of rows is one contiguous run of both.  One
-// CTA per token, one warp per group at a time, 4 channels per lane.
+// to sxT[g][row], so one tile of rows is one contiguous run of both.  CTA
+// (token, blockIdx.y) quantises groups 8*blockIdx.y .. +7, one warp per
+// group, 4 channels per lane.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __restrict__ x, int T, int H, int k,
                                                             int n_shared, const int32_t* __restrict__ inv_int,
@@ -544,7 +587,7 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __re
     if (threadIdx.x == 0 && n_shared) dest[k] = offsets_pad[E] + t;
     __syncthreads();
     const int G = H / QB;
-    for (int g = warp; g < G; g += 8) {
+    for (int g = blockIdx.y * 8 + warp; g < G; g += 8 * gridDim.y) {
         const uint2 raw = *reinterpret_cast<const uint2*>(x + (size_t)t * H + g * QB + lane * 4);
         const float v0 = __uint_as_float(raw.x << 16), v1 = __uint_as_float(raw.x & 0xFFFF0000u);
         const float v2 = __uint_as_float(raw.y << 16), v3 = __uint_as_float(raw.y & 0xFFFF0000u);
@@ -567,7 +610,9 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __re
 cudaError_t launch_quant_scatter(const moe_layer* L, const uint16_t* x, int T, const WsLayout& lay, char* ws,
                                  uint8_t* xq_out, float* sx_out, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    quant_scatter_kernel<<<T, 256, 0, s>>>(x, T, L->d.hidden, L->d.top_k, L->d.n_shared,
+    // one warp per 128-channel group: grid.y covers the groups 8 at a time
+    const dim3 grid(T, (L->d.hidden / QB + 7) / 8);
+    quant_scatter_kernel<<<grid, 256, 0, s>>>(x, T, L->d.hidden, L->d.top_k, L->d.n_shared,
                                            reinterpret_cast<const int32_t*>(ws + lay.inv_int),
                                            reinterpret_cast<const int32_t*>(ws + lay.offsets_pad), L->d.n_experts,
                                            reinterpret_cast<uint8_t*>(ws + lay.xp),
