@@ -45,18 +45,11 @@ moe::WsLayout make_layout(const moe_layer* L, int T, int mode) {
     // internal rows: every routed group padded to ROW_ALIGN, then the shared group
     const size_t rows = R + (L->d.n_shared ? (size_t)T : 0) + (size_t)moe::ROW_ALIGN * (E + 1);
     l.rows_pad = (int)up(rows + moe::ROW_PAD, 64);
-    // router: T <= 64 -> the split GEMV; otherwise the tiled GEMM, split
-    // along H (a divisor of H/128) until the grid covers ~2 waves.  Either
-    // way ksplit partial sums, added in order by the top-k kernel.
+    // router: T <= 64 -> the split GEMV; otherwise the tensor-core GEMM,
+    // split along H.  Either way ksplit partial sums, added in order by the
+    // top-k kernel.
     l.gemv = T <= 64;
-    if (l.gemv) {
-        l.ksplit = moe::router_gemv_splits((int)H);
-    } else {
-        const int base = (int)((E + 63) / 64) * ((T + 63) / 64), hb = (int)(H / moe::QB);
-        l.ksplit = 1;
-        for (int d = 1; d <= hb; ++d)
-            if (hb % d == 0 && base * d <= 2 * L->num_sms) l.ksplit = d;
-    }
+    l.ksplit = l.gemv ? moe::router_gemv_splits((int)H) : moe::router_tc_splits(T, (int)H, (int)E, L->num_sms);
     l.n_chunks = (T + moe::CHUNK_TOK - 1) / moe::CHUNK_TOK;
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t o = off; off = up(off + bytes, 256); return o; };
@@ -230,7 +223,7 @@ MOE_EXPORT moe_status moe_create(const moe_desc* d, const moe_weights* w, void* 
     L->wait_limit = kDefaultWaitLimitUs;
     auto cleanup = [&](moe_status st) {
         cudaFree(L->w_gu); cudaFree(L->w_dn); cudaFree(L->s_gu); cudaFree(L->s_dn); cudaFree(L->r_gu); cudaFree(L->r_dn);
-        cudaFree(L->router_w); cudaFree(L->router_b); cudaFree(L->dev_status);
+        cudaFree(L->router_w); cudaFree(L->router_w3); cudaFree(L->router_b); cudaFree(L->dev_status);
         delete L;
         return st;
     };
@@ -249,6 +242,8 @@ MOE_EXPORT moe_status moe_create(const moe_desc* d, const moe_weights* w, void* 
     if ((e = cudaMalloc(&L->r_gu, rgu)) != cudaSuccess) return cleanup(cuda_fail(e, "allocating scale records"));
     if ((e = cudaMalloc(&L->r_dn, rdn)) != cudaSuccess) return cleanup(cuda_fail(e, "allocating scale records"));
     if ((e = cudaMalloc(&L->router_w, E * H * 4)) != cudaSuccess) return cleanup(cuda_fail(e, "allocating router"));
+    if ((e = cudaMalloc(&L->router_w3, moe::router_split_bytes(L))) != cudaSuccess)
+        return cleanup(cuda_fail(e, "allocating router terms"));
     if ((e = cudaMalloc(&L->router_b, E * 4)) != cudaSuccess) return cleanup(cuda_fail(e, "allocating bias"));
     if ((e = cudaMalloc(&L->dev_status, 4)) != cudaSuccess) return cleanup(cuda_fail(e, "allocating status"));
     if ((e = cudaMemsetAsync(L->dev_status, 0, 4, s)) != cudaSuccess) return cleanup(cuda_fail(e, "memset"));
@@ -257,6 +252,7 @@ MOE_EXPORT moe_status moe_create(const moe_desc* d, const moe_weights* w, void* 
     e = w->router_bias ? cudaMemcpyAsync(L->router_b, w->router_bias, E * 4, cudaMemcpyDeviceToDevice, s)
                        : cudaMemsetAsync(L->router_b, 0, E * 4, s);
     if (e != cudaSuccess) return cleanup(cuda_fail(e, "copying router bias"));
+    if ((e = moe::launch_split_router_weights(L, s)) != cudaSuccess) return cleanup(cuda_fail(e, "router split"));
     if ((e = moe::launch_repack(L, w, s)) != cudaSuccess) return cleanup(cuda_fail(e, "weight repack"));
     if ((e = moe::launch_tc_scale_records(L, s)) != cudaSuccess) return cleanup(cuda_fail(e, "scale records"));
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cleanup(cuda_fail(e, "moe_create synchronise"));
@@ -270,7 +266,7 @@ MOE_EXPORT moe_status moe_destroy(moe_layer* L) {
     if (L->profile)
         for (cudaEvent_t ev : L->ev) cudaEventDestroy(ev);
     cudaFree(L->w_gu); cudaFree(L->w_dn); cudaFree(L->s_gu); cudaFree(L->s_dn); cudaFree(L->r_gu); cudaFree(L->r_dn);
-    cudaFree(L->router_w); cudaFree(L->router_b); cudaFree(L->dev_status);
+    cudaFree(L->router_w); cudaFree(L->router_w3); cudaFree(L->router_b); cudaFree(L->dev_status);
     delete L;
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_destroy synchronise");
 }

@@ -152,6 +152,7 @@ struct moe_layer {
     float* r_gu;           // [G][I/128][H/128][4]: {gate, up, 0, 0} per k block (16-byte records)
     float* r_dn;           // [G][ceil(H/256)][I/128][4]: {s(2b), s(2b+1) or 0, 0, 0} per k block
     float* router_w;       // [E][H]
+    uint16_t* router_w3;   // [3][E][H] bf16 terms of router_w (w = w1 + w2 + w3), prefill router GEMM
     float* router_b;       // [E] (zeros when no bias)
     uint32_t* dev_status;  // device status word
     uint32_t wait_limit;
@@ -297,6 +298,10 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(
 namespace moe {
 cudaError_t launch_repack(const moe_layer* L, const moe_weights* w, cudaStream_t s);
 int router_gemv_splits(int H);
+int router_tc_splits(int T, int H, int E, int num_sms);
+size_t router_split_bytes(const moe_layer* L);
+cudaError_t launch_split_router_weights(const moe_layer* L, cudaStream_t s);
+cudaError_t launch_router_tc(const moe_layer* L, const uint16_t* x, int T, float* part, int ksplit, cudaStream_t s);
 cudaError_t launch_router_logits(const moe_layer* L, const uint16_t* x, int T, float* part, int ksplit, bool gemv,
                                  cudaStream_t s);
 cudaError_t launch_topk(const moe_layer* L, const float* part, int ksplit, bool add_bias, int T, float* logits_out,

@@ -15,105 +15,6 @@
 namespace moe {
 
 // ---------------------------------------------------------------------------
-// Router logits: part[z][t][e] = sum_{h in split z} x[t][h] * Wr[e][h]
-// (fp32 FMA; each 32-wide K step is summed into a fresh partial before it is
-// added to the running total, which keeps the rounding error near
-// sqrt(H/32) ulp).  The bias and the sum over splits are added by the top-k
-// kernel in a fixed order.  Tile: 64 tokens x 64 experts per CTA, 4x4 per
-// thread; split z covers H/ksplit consecutive channels (grid.z = ksplit, so
-// a decode batch still spreads the router weights over >= 152 CTAs).
-// ---------------------------------------------------------------------------
-constexpr int LT = 64, LE = 64, LK = 32;
-
-__global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __restrict__ x,
-                                                            const float* __restrict__ W, int T, int H, int E,
-                                                            int kchunk, float* __restrict__ part) {
-    __shared__ float xs[LK][LT + 4];
-    __shared__ float ws[LK][LE + 4];
-    const int tid = threadIdx.x;
-    const int tx = tid & 15, ty = tid >> 4;
-    const int t0 = blockIdx.y * LT, e0 = blockIdx.x * LE;
-    const int z = blockIdx.z;
-    const int kbeg = z * kchunk, kend = kbeg + kchunk;
-    float acc[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-
-    const int lr = tid >> 2;          // row (token / expert) this thread loads
-    const int lc = (tid & 3) * 8;     // 8 consecutive channels
-    for (int k0 = kbeg; k0 < kend; k0 += LK) {
-        {
-            const int t = t0 + lr;
-            float v[8];
-            if (t < T) {
-                uint4 raw = *reinterpret_cast<const uint4*>(x + (size_t)t * H + k0 + lc);
-                const uint32_t wds[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    v[2 * i] = __uint_as_float(wds[i] << 16);
-                    v[2 * i + 1] = __uint_as_float(wds[i] & 0xFFFF0000u);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = 0.f;
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) xs[lc + i][lr] = v[i];
-        }
-        {
-            const int e = e0 + lr;
-            float v[8];
-            if (e < E) {
-                const float4* src = reinterpret_cast<const float4*>(W + (size_t)e * H + k0 + lc);
-                float4 a = src[0], b = src[1];
-                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-                v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = 0.f;
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) ws[lc + i][lr] = v[i];
-        }
-        __syncthreads();
-        float p[4][4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) p[i][j] = 0.f;
-#pragma unroll 8
-        for (int kk = 0; kk < LK; ++kk) {
-            float a[4], b[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) a[i] = xs[kk][ty * 4 + i];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) b[j] = ws[kk][tx * 4 + j];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) p[i][j] = __fmaf_rn(a[i], b[j], p[i][j]);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] = __fadd_rn(acc[i][j], p[i][j]);
-        __syncthreads();
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int t = t0 + ty * 4 + i;
-        if (t >= T) continue;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e = e0 + tx * 4 + j;
-            if (e < E) part[((size_t)z * T + t) * E + e] = acc[i][j];
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
 // Router logits for a decode batch (T <= 64): a GEMV over the fp32 router
 // weights, which dominate the bytes.  The channels are split into ksplit
 // slices (grid.y); a CTA stages its slice of x for up to GEMV_TC tokens in
@@ -211,9 +112,7 @@ cudaError_t launch_router_logits(const moe_layer* L, const uint16_t* x, int T, f
         router_gemv_kernel<<<grid, GEMV_WARPS * 32, smem, s>>>(x, L->router_w, T, H, E, slice, tc, part);
         return cudaGetLastError();
     }
-    dim3 grid((E + LE - 1) / LE, (T + LT - 1) / LT, ksplit);
-    router_logits_kernel<<<grid, 256, 0, s>>>(x, L->router_w, T, H, E, H / ksplit, part);
-    return cudaGetLastError();
+    return launch_router_tc(L, x, T, part, ksplit, s);      // prefill batch: tensor-core GEMM (router_tc.cu)
 }
 
 // ---------------------------------------------------------------------------
