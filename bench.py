@@ -311,7 +311,7 @@ def run_ours(a, wl):
         else:
             alg = n_touched * (H * wl.inter + (H // 128) * (wl.inter // 128) * 4) + rows * (wl.inter + 4 * H)
         achieved = alg / dom_s / 1e9
-        roof = {"bound": "hbm", "kernel": f"expert_gemm_kernel<{'true' if dom == 'gate_up' else 'false'}>",
+        roof = {"bound": "hbm", "kernel": f"moe::expert_gemm_kernel<{1 if dom == 'gate_up' else 0}> ({dom})",
                 "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s", "frac": achieved / pk["hbm"],
                 "algorithmic_bytes_per_launch": alg, "peak_source": pk["src"],
                 "traffic": traffic_for(dom, wl.name)}
@@ -320,11 +320,23 @@ def run_ours(a, wl):
         alg = flops_all * (2 / 3 if dom == "gate_up" else 1 / 3)
         achieved = alg / dom_s / 1e12
         peak = pk["bf16"] * FP8_OVER_BF16
-        roof = {"bound": "tensor", "kernel": f"expert_gemm_kernel<{'true' if dom == 'gate_up' else 'false'}>",
+        roof = {"bound": "tensor", "kernel": f"tc::expert_tc_kernel<{1 if dom == 'gate_up' else 0}> ({dom})",
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "algorithmic_flops_per_launch": alg,
                 "peak_source": f"{pk['src']} bf16 burst x {FP8_OVER_BF16} (nominal fp8/bf16 dense ratio)",
                 "traffic": traffic_for(dom, wl.name)}
+
+    # ---------------------------------------------- the whole layer against the same peak (the targets are
+    # stated per layer: touched-expert bytes / layer time for decode, expert FLOP / layer time for prefill)
+    if is_decode(wl):
+        lb = roofline.decode_weight_bytes(ids_np, H, wl.inter, wl.n_experts, wl.n_shared)
+        layer_roof = {"bound": "hbm", "algorithmic_bytes": lb, "achieved": lb / sec_per_step / 1e9,
+                      "peak": pk["hbm"], "unit": "GB/s", "frac": lb / sec_per_step / 1e9 / pk["hbm"]}
+    else:
+        lf = roofline.layer_flops(T, H, wl.inter, wl.top_k, wl.n_shared)
+        layer_roof = {"bound": "tensor", "algorithmic_flops": lf, "achieved": lf / sec_per_step / 1e12,
+                      "peak": pk["bf16"] * FP8_OVER_BF16, "unit": "TFLOP/s",
+                      "frac": lf / sec_per_step / 1e12 / (pk["bf16"] * FP8_OVER_BF16)}
 
     # ---------------------------------------------- end to end through the host entry
     e2e = None
@@ -366,7 +378,8 @@ def run_ours(a, wl):
             "config": {"workload": wl.name, "T": T, "hidden": H, "inter": wl.inter, "n_experts": wl.n_experts,
                        "top_k": wl.top_k, "n_shared": wl.n_shared, "parallelism": f"replicas{world}",
                        "l2": "flushed between steps (512 MiB write, outside the timed events)"},
-            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_launches * world,
+            "roofline": roof, "layer_roofline": layer_roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": n_launches * world,
             "clocks": clk.summary(), "stage_ms": mean_stage, "touched_experts": n_touched,
             "wall_s_timed_region": t_wall, "tokens_per_s": T * world / sec_per_step,
         }
