@@ -59,6 +59,9 @@ def parse():
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--layers", type=int, default=1,
+                   help="> 1: time a stack of this many layers (distinct weight copies in HBM, distinct routers), "
+                        "captured as one CUDA graph; the metric is then per layer")
     a = p.parse_args()
     a.warmup = max(a.warmup, 3)
     if a.steps is None:
@@ -389,11 +392,103 @@ def run_ours(a, wl):
     return 0
 
 
+def run_layers(a, wl):
+    """A stack of a.layers layers run as one CUDA graph replay per step
+    (moe_forward_layers inside LayerStackGraph).  Every layer is its own copy
+    of the expert weights in HBM with its own router (seed + l), so each
+    layer routes its input differently; the input of layer l + 1 is the
+    output of layer l."""
+    import torch
+    import moe_expert_ffn_02_gb300 as moe
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    moe.load()
+    metric, unit, hib = metric_of(wl)
+    inp = synth.make_inputs(wl, seed=a.seed)
+    dev = {k: (torch.from_numpy(np.ascontiguousarray(v)).cuda() if v is not None else None)
+           for k, v in inp.items() if k != "x"}
+    layers = []
+    for l in range(a.layers):
+        if l:
+            rstd = wl.router_std if wl.router_std is not None else 1.0 / np.sqrt(wl.hidden)
+            dev["router_w"] = torch.from_numpy(
+                synth.f32_normal(a.seed + l, synth.STREAM_ROUTER_W, (wl.n_experts, wl.hidden), float(rstd))).cuda()
+        layers.append(moe.Layer(wl.hidden, wl.inter, wl.n_experts, wl.top_k, dev, n_shared=wl.n_shared))
+    del dev
+    torch.cuda.empty_cache()
+    T, H = wl.T, wl.hidden
+    mode = moe.MODE_DECODE if is_decode(wl) else moe.MODE_PREFILL
+    x = torch.from_numpy(inp["x"].view(np.int16)).cuda()
+    y = torch.empty_like(x)
+
+    # per-layer routing of the chained inputs, for the touched-byte count
+    touched_bytes, xi = 0, x.clone()
+    for ly in layers:
+        ids = torch.empty((T, wl.top_k), dtype=torch.int32, device="cuda")
+        ws, nb = ly.workspace(T, mode)
+        yi = torch.empty_like(xi)
+        moe.moe_forward_prefill(ly.handle, xi.data_ptr(), T, yi.data_ptr(), {"topk_ids": ids.data_ptr()}, ws, nb,
+                                torch.cuda.current_stream().cuda_stream)
+        touched_bytes += roofline.decode_weight_bytes(ids.cpu().numpy(), H, wl.inter, wl.n_experts, wl.n_shared)
+        xi = yi
+    g = moe.LayerStackGraph([ly.handle for ly in layers], mode, x, y)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    for _ in range(a.warmup):
+        flush.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
+    cur = torch.cuda.current_stream()          # the graph replays on the current stream
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
+        for i in range(a.steps):
+            flush.zero_()
+            starts[i].record(cur)
+            g.replay()
+            ends[i].record(cur)
+        torch.cuda.synchronize()
+    sec_per_step = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / a.steps / 1e3
+    for ly in layers:
+        st, flags = moe.moe_get_device_status(ly.handle, 0)
+        if st != 0:
+            raise RuntimeError(f"device status {st} flags {flags:#x}")
+    pk = peaks()
+    per_layer = sec_per_step / a.layers
+    if is_decode(wl):
+        achieved = touched_bytes / sec_per_step / 1e9
+        roof = {"bound": "hbm", "kernel": f"stack of {a.layers} layers (one CUDA graph)", "achieved": achieved,
+                "peak": pk["hbm"], "unit": "GB/s", "frac": achieved / pk["hbm"],
+                "algorithmic_bytes_per_launch": touched_bytes, "peak_source": pk["src"], "traffic": None}
+    else:
+        lf = roofline.layer_flops(T, H, wl.inter, wl.top_k, wl.n_shared) * a.layers
+        achieved = lf / sec_per_step / 1e12
+        peak = pk["bf16"] * FP8_OVER_BF16
+        roof = {"bound": "tensor", "kernel": f"stack of {a.layers} layers (one CUDA graph)", "achieved": achieved,
+                "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "algorithmic_flops_per_launch": lf,
+                "peak_source": f"{pk['src']} bf16 burst x {FP8_OVER_BF16} (nominal fp8/bf16 dense ratio)",
+                "traffic": None}
+    line = {
+        "metric": metric, "value": value_of(wl, per_layer, 1), "unit": unit, "n_gpus": 1, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": sec_per_step * 1e3, "higher_is_better": hib, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8_e4m3", "data": "synthetic",
+        "config": {"workload": wl.name, "T": T, "hidden": H, "inter": wl.inter, "n_experts": wl.n_experts,
+                   "top_k": wl.top_k, "n_shared": wl.n_shared, "parallelism": "replicas1", "layers": a.layers,
+                   "graph": True, "l2": "flushed between steps (512 MiB write, outside the timed events)"},
+        "roofline": roof, "cpu_baseline": None, "e2e": None, "gpu_launches": 9 * a.layers * a.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    for ly in layers:
+        ly.close()
+    return 0
+
+
 def main():
     a = parse()
     wl = synth.WORKLOADS[a.workload]
     if a.impl == "reference":
         return run_reference(a, wl)
+    if a.layers > 1:
+        return run_layers(a, wl)
     return run_ours(a, wl)
 
 

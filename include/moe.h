@@ -199,6 +199,52 @@ moe_status moe_forward_decode(moe_layer* layer, const uint16_t* x, int32_t T, ui
 moe_status moe_forward_host(moe_layer* layer, int32_t mode, const uint16_t* x_host, int32_t T,
                             uint16_t* y_host, void* ws, size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------- variants
+ * The three entries below reuse the layer's kernels and change only how the
+ * work is composed or combined. */
+
+/* A stack of MoE layers as one call: layer l's output y is layer l+1's
+ * input x ("LLM serving on heterogeneous hardware" lecture, section 4.3,
+ * and KTransformers deep dive, section 2.4: a decode step runs every layer
+ * back to back and is recorded as one CUDA graph).  mode: MOE_MODE_PREFILL or
+ * MOE_MODE_DECODE for every layer.  `layers` is a host array of n_layers
+ * handles, all with the same hidden size (they may be the same handle).
+ * x, y: device [T][H] bf16.  The call enqueues work only (no host
+ * synchronisation), so it can be captured into a CUDA graph.  Workspace:
+ * moe_layers_workspace_bytes (the largest single-layer workspace plus two
+ * T x H bf16 carry buffers).  Errors as for moe_forward_prefill. */
+moe_status moe_layers_workspace_bytes(moe_layer* const* layers, int32_t n_layers, int32_t T, int32_t mode,
+                                      size_t* bytes);
+moe_status moe_forward_layers(moe_layer* const* layers, int32_t n_layers, int32_t mode, const uint16_t* x,
+                              int32_t T, uint16_t* y, void* ws, size_t ws_bytes, void* stream);
+
+/* The layer with the SmallEP combine emulated on one GPU (CPU-GPU hybrid
+ * inference article, SmallEP section, Fig. 5: expert-parallel ranks each
+ * combine their own experts, then the partial outputs are reduced).  The
+ * routed experts are split into n_ranks contiguous groups, rank p holding
+ * experts [ceil(pE/n_ranks), ceil((p+1)E/n_ranks)) and rank 0 also the
+ * shared expert.  Each rank's partial is the fixed-order fp32 sum of its
+ * slots; y = bf16 of the partials added in rank order.  n_ranks = 1 gives
+ * bit for bit the output of moe_forward_prefill / moe_forward_decode; other
+ * n_ranks are deterministic but round differently.  1 <= n_ranks <= E.
+ * Workspace and errors as for the mode's entry. */
+moe_status moe_forward_smallep(moe_layer* layer, int32_t mode, int32_t n_ranks, const uint16_t* x, int32_t T,
+                               uint16_t* y, void* ws, size_t ws_bytes, void* stream);
+
+/* Expert deferral ("LLM serving on heterogeneous hardware" lecture, section
+ * 4.3: the results of some selected experts join the residual stream one
+ * layer later, so the next layer can start; the lecture keeps at least two
+ * experts per token undeferred, a policy left to the caller here).  defer: device uint8 [T][k], slot j of token t deferred
+ * when non-zero, slots in the rank order of topk_ids.  Outputs, device
+ * [T][H] bf16: y_now = O[shared] + the non-deferred w_j O_j, y_next = the
+ * deferred w_j O_j, each summed in slot order in fp32 and rounded once.  All
+ * experts are still computed in this call; the split is in the combine.
+ * With no slot deferred, y_now equals moe_forward_* bit for bit and y_next
+ * is zero.  Workspace and errors as for the mode's entry; y_next must be
+ * 16-byte aligned. */
+moe_status moe_forward_deferred(moe_layer* layer, int32_t mode, const uint16_t* x, int32_t T, const uint8_t* defer,
+                                uint16_t* y_now, uint16_t* y_next, void* ws, size_t ws_bytes, void* stream);
+
 /* Synchronise `stream`, then read and clear the device status word
  * (MOE_DEV_* bits).  Returns MOE_ERR_TIMEOUT if the timeout bit was set,
  * MOE_ERR_DEVICE_CHECK for any other bit, MOE_OK when clear. */

@@ -22,7 +22,8 @@ __all__ = [
     "DECODE_MAX_T", "moe_create", "moe_destroy", "moe_workspace_bytes", "moe_route", "moe_route_from_logits",
     "moe_route_from_logits_noalloc", "moe_forward_prefill", "moe_forward_decode", "moe_forward_host", "moe_get_device_status",
     "moe_set_wait_limit", "moe_debug_timeout_probe", "moe_profile_enable", "moe_profile_read", "moe_status_string", "moe_last_error",
-    "moe_abi_version", "library_path", "load", "Layer",
+    "moe_abi_version", "moe_forward_smallep", "moe_forward_deferred", "moe_layers_workspace_bytes",
+    "moe_forward_layers", "smallep_groups", "library_path", "load", "Layer", "LayerStackGraph",
 ]
 
 MODE_ROUTE, MODE_PREFILL, MODE_DECODE = 0, 1, 2
@@ -91,6 +92,10 @@ def load(build_if_missing: bool = False):
             "moe_set_wait_limit": ([vp, u32], st),
             "moe_debug_timeout_probe": ([vp, vp], st),
             "moe_route_from_logits_noalloc": ([vp, vp, i32, ctypes.POINTER(MoeRouteOut), vp], st),
+            "moe_forward_smallep": ([vp, i32, i32, vp, i32, vp, vp, sz, vp], st),
+            "moe_forward_deferred": ([vp, i32, vp, i32, vp, vp, vp, vp, sz, vp], st),
+            "moe_layers_workspace_bytes": ([ctypes.POINTER(vp), i32, i32, i32, ctypes.POINTER(sz)], st),
+            "moe_forward_layers": ([ctypes.POINTER(vp), i32, i32, vp, i32, vp, vp, sz, vp], st),
             "moe_profile_enable": ([vp, i32], st),
             "moe_profile_read": ([vp, ctypes.POINTER(ctypes.c_float), i32], st),
             "moe_status_string": ([st], ctypes.c_char_p),
@@ -177,6 +182,39 @@ def moe_forward_host(layer: int, mode: int, x_host: int, T: int, y_host: int, ws
     _check(load().moe_forward_host(layer, mode, x_host, T, y_host, ws, ws_bytes, stream))
 
 
+def moe_forward_smallep(layer: int, mode: int, n_ranks: int, x: int, T: int, y: int, ws: int, ws_bytes: int,
+                        stream: int = 0) -> None:
+    _check(load().moe_forward_smallep(layer, mode, n_ranks, x, T, y, ws, ws_bytes, stream))
+
+
+def smallep_groups(n_experts: int, n_ranks: int):
+    """Expert range [lo, hi) of each SmallEP rank, as moe_forward_smallep
+    splits them: rank p holds [ceil(p E / P), ceil((p + 1) E / P)); rank 0
+    also holds the shared expert."""
+    b = [(p * n_experts + n_ranks - 1) // n_ranks for p in range(n_ranks + 1)]
+    return [(b[p], b[p + 1]) for p in range(n_ranks)]
+
+
+def moe_forward_deferred(layer: int, mode: int, x: int, T: int, defer: int, y_now: int, y_next: int, ws: int,
+                         ws_bytes: int, stream: int = 0) -> None:
+    _check(load().moe_forward_deferred(layer, mode, x, T, defer, y_now, y_next, ws, ws_bytes, stream))
+
+
+def _handles(layers):
+    arr = (ctypes.c_void_p * len(layers))(*[int(h) for h in layers])
+    return arr
+
+
+def moe_layers_workspace_bytes(layers, T: int, mode: int) -> int:
+    n = ctypes.c_size_t()
+    _check(load().moe_layers_workspace_bytes(_handles(layers), len(layers), T, mode, ctypes.byref(n)))
+    return n.value
+
+
+def moe_forward_layers(layers, mode: int, x: int, T: int, y: int, ws: int, ws_bytes: int, stream: int = 0) -> None:
+    _check(load().moe_forward_layers(_handles(layers), len(layers), mode, x, T, y, ws, ws_bytes, stream))
+
+
 def moe_get_device_status(layer: int, stream: int = 0):
     """Returns (status, flags) without raising, so callers can inspect both."""
     f = ctypes.c_uint32()
@@ -248,3 +286,34 @@ class Layer:
             self.close()
         except Exception:
             pass
+
+
+class LayerStackGraph:
+    """A stack of layers (handles) run as one moe_forward_layers call,
+    captured once into a CUDA graph and replayed: the whole decode step is a
+    single graph launch.  x and y are torch CUDA bf16-bits tensors [T][H]
+    owned by the caller; replay() runs the stack on the current contents of
+    x and leaves the result in y."""
+
+    def __init__(self, handles, mode: int, x, y, warmup: int = 1):
+        import torch
+        self.handles = list(handles)
+        self.mode = mode
+        self.x, self.y = x, y
+        T = x.shape[0]
+        need = moe_layers_workspace_bytes(self.handles, T, mode)
+        self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+        self.stream = torch.cuda.Stream(device=x.device)
+        run = lambda: moe_forward_layers(self.handles, mode, x.data_ptr(), T, y.data_ptr(), self.ws.data_ptr(),
+                                         self.ws.numel(), self.stream.cuda_stream)
+        with torch.cuda.stream(self.stream):
+            for _ in range(warmup):           # one-time kernel attributes are set outside the capture
+                run()
+        self.stream.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            run()
+
+    def replay(self):
+        """Launch the captured stack on the current torch stream."""
+        self.graph.replay()

@@ -2,6 +2,7 @@
 // workspace carve-up, layer ownership and the launch sequence of each entry.
 #include "moe_internal.cuh"
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <string>
@@ -130,8 +131,16 @@ moe_status run_route(moe_layer* L, const uint16_t* x, const float* logits_in, in
     return MOE_OK;
 }
 
+// How the expert outputs are combined: the plain fixed-order sum, the SmallEP
+// partial sums over n_ranks expert groups, or the deferral split.
+struct CombineSpec {
+    int n_ranks = 1;
+    const uint8_t* defer = nullptr;
+    uint16_t* y_next = nullptr;
+};
+
 moe_status run_forward(moe_layer* L, int mode, const uint16_t* x, int T, uint16_t* y, const moe_route_out* dbg,
-                       void* ws_v, size_t ws_bytes, cudaStream_t s) {
+                       void* ws_v, size_t ws_bytes, cudaStream_t s, const CombineSpec& cs = CombineSpec()) {
     moe::WsLayout lay;
     moe_status st = check_call(L, T, mode, x, y, ws_v, ws_bytes, &lay);
     if (st != MOE_OK) return st;
@@ -163,7 +172,10 @@ moe_status run_forward(moe_layer* L, int mode, const uint16_t* x, int T, uint16_
     MOE_CUDA(tc_path ? moe::launch_expert_tc_down(L, T, lay, ws, s) : moe::launch_expert_down(L, T, lay, ws, kBN, 0, s),
              "down GEMM");
     MOE_CUDA(mark(4), "profile event");
-    MOE_CUDA(moe::launch_combine(L, T, lay, ws, y, s), "combine");
+    if (cs.n_ranks == 1 && !cs.defer)
+        MOE_CUDA(moe::launch_combine(L, T, lay, ws, y, s), "combine");
+    else
+        MOE_CUDA(moe::launch_combine_split(L, T, lay, ws, cs.n_ranks, cs.defer, y, cs.y_next, s), "combine");
     MOE_CUDA(mark(5), "profile event");
     return MOE_OK;
 }
@@ -319,6 +331,81 @@ MOE_EXPORT moe_status moe_forward_prefill(moe_layer* L, const uint16_t* x, int32
 MOE_EXPORT moe_status moe_forward_decode(moe_layer* L, const uint16_t* x, int32_t T, uint16_t* y,
                                          const moe_route_out* dbg, void* ws, size_t ws_bytes, void* stream) {
     return run_forward(L, MOE_MODE_DECODE, x, T, y, dbg, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+MOE_EXPORT moe_status moe_forward_smallep(moe_layer* L, int32_t mode, int32_t n_ranks, const uint16_t* x, int32_t T,
+                                          uint16_t* y, void* ws, size_t ws_bytes, void* stream) {
+    moe_status st = check_layer(L);
+    if (st != MOE_OK) return st;
+    if (mode != MOE_MODE_PREFILL && mode != MOE_MODE_DECODE) return fail(MOE_ERR_INVALID_ARG, "mode must be 1 or 2");
+    if (n_ranks < 1 || n_ranks > L->d.n_experts)
+        return fail(MOE_ERR_INVALID_ARG, "n_ranks (%d) must be in [1, n_experts]", n_ranks);
+    CombineSpec cs;
+    cs.n_ranks = n_ranks;
+    return run_forward(L, mode, x, T, y, nullptr, ws, ws_bytes, static_cast<cudaStream_t>(stream), cs);
+}
+
+MOE_EXPORT moe_status moe_forward_deferred(moe_layer* L, int32_t mode, const uint16_t* x, int32_t T,
+                                           const uint8_t* defer, uint16_t* y_now, uint16_t* y_next, void* ws,
+                                           size_t ws_bytes, void* stream) {
+    moe_status st = check_layer(L);
+    if (st != MOE_OK) return st;
+    if (mode != MOE_MODE_PREFILL && mode != MOE_MODE_DECODE) return fail(MOE_ERR_INVALID_ARG, "mode must be 1 or 2");
+    if (T > 0 && (!defer || !y_next || !aligned(y_next, 16)))
+        return fail(MOE_ERR_INVALID_ARG, "defer and a 16-byte aligned y_next are required");
+    CombineSpec cs;
+    cs.defer = defer;
+    cs.y_next = y_next;
+    return run_forward(L, mode, x, T, y_now, nullptr, ws, ws_bytes, static_cast<cudaStream_t>(stream), cs);
+}
+
+namespace {
+// Workspace of a layer stack: the largest single-layer workspace, then two
+// T x H bf16 activation buffers that carry y of layer l to layer l + 1.
+moe_status layers_layout(moe_layer* const* layers, int n, int T, int mode, size_t* fwd, size_t* act) {
+    if (!layers || n < 1) return fail(MOE_ERR_INVALID_ARG, "layers must be non-NULL and n_layers >= 1");
+    if (mode != MOE_MODE_PREFILL && mode != MOE_MODE_DECODE) return fail(MOE_ERR_INVALID_ARG, "mode must be 1 or 2");
+    if (T < 0 || (mode == MOE_MODE_DECODE && T > MOE_DECODE_MAX_T)) return fail(MOE_ERR_INVALID_ARG, "bad T (%d)", T);
+    *fwd = 0;
+    for (int l = 0; l < n; ++l) {
+        if (!layers[l]) return fail(MOE_ERR_INVALID_ARG, "layer %d is NULL", l);
+        if (layers[l]->d.hidden != layers[0]->d.hidden)
+            return fail(MOE_ERR_INVALID_ARG, "layer %d has hidden %d, layer 0 has %d", l, layers[l]->d.hidden,
+                        layers[0]->d.hidden);
+        *fwd = std::max(*fwd, make_layout(layers[l], T, mode).total);
+    }
+    *act = up((size_t)T * layers[0]->d.hidden * 2, 256);
+    return MOE_OK;
+}
+}  // namespace
+
+MOE_EXPORT moe_status moe_layers_workspace_bytes(moe_layer* const* layers, int32_t n_layers, int32_t T, int32_t mode,
+                                                 size_t* bytes) {
+    size_t fwd = 0, act = 0;
+    moe_status st = layers_layout(layers, n_layers, T, mode, &fwd, &act);
+    if (st != MOE_OK) return st;
+    if (!bytes) return fail(MOE_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = fwd + 2 * act;
+    return MOE_OK;
+}
+
+MOE_EXPORT moe_status moe_forward_layers(moe_layer* const* layers, int32_t n_layers, int32_t mode, const uint16_t* x,
+                                         int32_t T, uint16_t* y, void* ws, size_t ws_bytes, void* stream) {
+    size_t fwd = 0, act = 0;
+    moe_status st = layers_layout(layers, n_layers, T, mode, &fwd, &act);
+    if (st != MOE_OK) return st;
+    if (!ws || !aligned(ws, 256)) return fail(MOE_ERR_INVALID_ARG, "workspace NULL or not 256-byte aligned");
+    if (ws_bytes < fwd + 2 * act) return fail(MOE_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, fwd + 2 * act);
+    char* base = static_cast<char*>(ws);
+    uint16_t* buf[2] = {reinterpret_cast<uint16_t*>(base + fwd), reinterpret_cast<uint16_t*>(base + fwd + act)};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    for (int l = 0; l < n_layers; ++l) {
+        const uint16_t* in = l == 0 ? x : buf[(l - 1) & 1];
+        uint16_t* out = l == n_layers - 1 ? y : buf[l & 1];
+        st = run_forward(layers[l], mode, in, T, out, nullptr, base, fwd, s);
+        if (st != MOE_OK) return st;
+    }
+    return MOE_OK;
 }
 
 MOE_EXPORT moe_status moe_forward_host(moe_layer* L, int32_t mode, const uint16_t* x_host, int32_t T,

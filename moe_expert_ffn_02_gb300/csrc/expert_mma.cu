@@ -411,6 +411,100 @@ cudaError_t launch_combine(const moe_layer* L, int T, const WsLayout& lay, char*
 }
 
 // ---------------------------------------------------------------------------
+// Split combines (same inputs as combine_kernel, same fp32 fused multiply-adds
+// in slot order inside each part).
+//
+// SmallEP partial sums (SmallEP section of the CPU-GPU hybrid inference
+// article, Fig. 5: each expert-parallel rank combines its own experts, then
+// the partial outputs are reduced): the routed experts are split into
+// n_ranks contiguous groups, rank p holding experts [ceil(p E / P),
+// ceil((p+1) E / P)) and rank 0 also the shared expert.  Part p = (p == 0 ?
+// O[shared] : 0) + sum over the slots j whose expert rank p holds, in slot
+// order, of w_j O[row_j]; y = bf16(((part_0 + part_1) + part_2) + ...).  With
+// one rank this is exactly combine_kernel.
+//
+// Deferral (when defer != NULL; n_ranks is then 1): the slots with
+// defer[t][j] != 0 go to y_next = bf16(sum of their w_j O[row_j]), the others
+// and the shared expert to y = bf16(O[shared] + sum of theirs).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) combine_split_kernel(const float* __restrict__ O,
+                                                            const int32_t* __restrict__ inv_int,
+                                                            const int32_t* __restrict__ ids,
+                                                            const float* __restrict__ w,
+                                                            const int32_t* __restrict__ offsets_pad,
+                                                            const uint8_t* __restrict__ defer, int T, int H, int k,
+                                                            int E, int n_shared, int n_ranks, uint16_t* __restrict__ y,
+                                                            uint16_t* __restrict__ y_next) {
+    __shared__ int rows[MAX_TOPK], part_of[MAX_TOPK];
+    __shared__ float wt[MAX_TOPK];
+    const int t = blockIdx.x;
+    if (threadIdx.x < k) {
+        const int j = threadIdx.x;
+        rows[j] = inv_int[(size_t)t * k + j];
+        wt[j] = w[(size_t)t * k + j];
+        if (defer) {
+            part_of[j] = defer[(size_t)t * k + j] ? 1 : 0;
+        } else {
+            const int e = min(max(ids[(size_t)t * k + j], 0), E - 1);
+            int p = 0;                              // largest p with ceil(p E / P) <= e
+            while (p + 1 < n_ranks && (int)(((long long)(p + 1) * E + n_ranks - 1) / n_ranks) <= e) ++p;
+            part_of[j] = p;
+        }
+    }
+    __syncthreads();
+    const int nparts = defer ? 2 : n_ranks;
+    const size_t shrow = (size_t)offsets_pad[E] + t;
+    for (int c = (blockIdx.y * blockDim.x + threadIdx.x) * 4; c < H; c += gridDim.y * blockDim.x * 4) {
+        float4 tot = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int p = 0; p < nparts; ++p) {
+            float4 acc = (p == 0 && n_shared) ? *reinterpret_cast<const float4*>(O + shrow * H + c)
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < k; ++j) {
+                if (part_of[j] != p) continue;
+                const float4 o = *reinterpret_cast<const float4*>(O + (size_t)rows[j] * H + c);
+                const float wj = wt[j];
+                acc.x = __fmaf_rn(wj, o.x, acc.x);
+                acc.y = __fmaf_rn(wj, o.y, acc.y);
+                acc.z = __fmaf_rn(wj, o.z, acc.z);
+                acc.w = __fmaf_rn(wj, o.w, acc.w);
+            }
+            if (defer) {
+                uint16_t* dst = (p == 0 ? y : y_next) + (size_t)t * H + c;
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+                const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+                *reinterpret_cast<uint2*>(dst) = make_uint2(*reinterpret_cast<const uint32_t*>(&lo),
+                                                            *reinterpret_cast<const uint32_t*>(&hi));
+            } else if (p == 0) {
+                tot = acc;
+            } else {
+                tot.x = __fadd_rn(tot.x, acc.x);
+                tot.y = __fadd_rn(tot.y, acc.y);
+                tot.z = __fadd_rn(tot.z, acc.z);
+                tot.w = __fadd_rn(tot.w, acc.w);
+            }
+        }
+        if (!defer) {
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(tot.x, tot.y);
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(tot.z, tot.w);
+            *reinterpret_cast<uint2*>(y + (size_t)t * H + c) = make_uint2(*reinterpret_cast<const uint32_t*>(&lo),
+                                                                           *reinterpret_cast<const uint32_t*>(&hi));
+        }
+    }
+}
+
+cudaError_t launch_combine_split(const moe_layer* L, int T, const WsLayout& lay, char* ws, int n_ranks,
+                                 const uint8_t* defer, uint16_t* y, uint16_t* y_next, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    const dim3 grid(T, (L->d.hidden + 1023) / 1024);
+    combine_split_kernel<<<grid, 256, 0, s>>>(
+        reinterpret_cast<const float*>(ws + lay.o), reinterpret_cast<const int32_t*>(ws + lay.inv_int),
+        reinterpret_cast<const int32_t*>(ws + lay.ids), reinterpret_cast<const float*>(ws + lay.w),
+        reinterpret_cast<const int32_t*>(ws + lay.offsets_pad), defer, T, L->d.hidden, L->d.top_k, L->d.n_experts,
+        L->d.n_shared, n_ranks, y, y_next);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // Debug copy of the h codes and scales per (token, slot), slots 0..k-1 the
 // routed experts in rank order and slot k the shared expert, unswizzled:
 // hq_out [T][S][I], sh_out [T][S][I/128].  One CTA per token.

@@ -321,6 +321,8 @@ cudaError_t launch_expert_tc_gate_up(const moe_layer* L, int T, const WsLayout& 
 cudaError_t launch_tc_scale_records(const moe_layer* L, cudaStream_t s);
 cudaError_t launch_expert_tc_down(const moe_layer* L, int T, const WsLayout& lay, char* ws, cudaStream_t s);
 cudaError_t launch_combine(const moe_layer* L, int T, const WsLayout& lay, char* ws, uint16_t* y, cudaStream_t s);
+cudaError_t launch_combine_split(const moe_layer* L, int T, const WsLayout& lay, char* ws, int n_ranks,
+                                 const uint8_t* defer, uint16_t* y, uint16_t* y_next, cudaStream_t s);
 cudaError_t launch_timeout_probe(const moe_layer* L, cudaStream_t s);
 void set_last_error(const char* msg);   // message returned by moe_last_error()
 }  // namespace moe
