@@ -62,6 +62,9 @@ def parse():
     p.add_argument("--layers", type=int, default=1,
                    help="> 1: time a stack of this many layers (distinct weight copies in HBM, distinct routers), "
                         "captured as one CUDA graph; the metric is then per layer")
+    p.add_argument("--host-tiles", action="store_true",
+                   help="with --layers: keep every layer's expert tiles in pinned host memory and stream them "
+                        "through a two-slot device ring while the previous layer computes")
     a = p.parse_args()
     a.warmup = max(a.warmup, 3)
     if a.steps is None:
@@ -412,7 +415,8 @@ def run_layers(a, wl):
             rstd = wl.router_std if wl.router_std is not None else 1.0 / np.sqrt(wl.hidden)
             dev["router_w"] = torch.from_numpy(
                 synth.f32_normal(a.seed + l, synth.STREAM_ROUTER_W, (wl.n_experts, wl.hidden), float(rstd))).cuda()
-        layers.append(moe.Layer(wl.hidden, wl.inter, wl.n_experts, wl.top_k, dev, n_shared=wl.n_shared))
+        layers.append(moe.Layer(wl.hidden, wl.inter, wl.n_experts, wl.top_k, dev, n_shared=wl.n_shared,
+                                host_tiles=a.host_tiles))
     del dev
     torch.cuda.empty_cache()
     T, H = wl.T, wl.hidden
@@ -422,7 +426,7 @@ def run_layers(a, wl):
 
     # per-layer routing of the chained inputs, for the touched-byte count
     touched_bytes, xi = 0, x.clone()
-    for ly in layers:
+    for ly in (layers if not a.host_tiles else []):
         ids = torch.empty((T, wl.top_k), dtype=torch.int32, device="cuda")
         ws, nb = ly.workspace(T, mode)
         yi = torch.empty_like(xi)
@@ -430,7 +434,12 @@ def run_layers(a, wl):
                                 torch.cuda.current_stream().cuda_stream)
         touched_bytes += roofline.decode_weight_bytes(ids.cpu().numpy(), H, wl.inter, wl.n_experts, wl.n_shared)
         xi = yi
-    g = moe.LayerStackGraph([ly.handle for ly in layers], mode, x, y)
+    if a.host_tiles:
+        g = moe.StreamedStack(layers, mode, x, y)
+        g.replay = g.run
+        tiles_bytes = moe.moe_tiles_bytes(layers[0].handle)
+    else:
+        g = moe.LayerStackGraph([ly.handle for ly in layers], mode, x, y)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     for _ in range(a.warmup):
         flush.zero_()
@@ -453,7 +462,7 @@ def run_layers(a, wl):
             raise RuntimeError(f"device status {st} flags {flags:#x}")
     pk = peaks()
     per_layer = sec_per_step / a.layers
-    if is_decode(wl):
+    if is_decode(wl) and not a.host_tiles:
         achieved = touched_bytes / sec_per_step / 1e9
         roof = {"bound": "hbm", "kernel": f"stack of {a.layers} layers (one CUDA graph)", "achieved": achieved,
                 "peak": pk["hbm"], "unit": "GB/s", "frac": achieved / pk["hbm"],
@@ -462,7 +471,9 @@ def run_layers(a, wl):
         lf = roofline.layer_flops(T, H, wl.inter, wl.top_k, wl.n_shared) * a.layers
         achieved = lf / sec_per_step / 1e12
         peak = pk["bf16"] * FP8_OVER_BF16
-        roof = {"bound": "tensor", "kernel": f"stack of {a.layers} layers (one CUDA graph)", "achieved": achieved,
+        roof = {"bound": "tensor", "achieved": achieved,
+                "kernel": f"stack of {a.layers} layers " + ("(two-slot host-tile ring)" if a.host_tiles else
+                                                            "(one CUDA graph)"),
                 "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "algorithmic_flops_per_launch": lf,
                 "peak_source": f"{pk['src']} bf16 burst x {FP8_OVER_BF16} (nominal fp8/bf16 dense ratio)",
                 "traffic": None}
@@ -476,6 +487,11 @@ def run_layers(a, wl):
         "roofline": roof, "cpu_baseline": None, "e2e": None, "gpu_launches": 9 * a.layers * a.steps,
         "clocks": clk.summary(),
     }
+    if a.host_tiles:
+        line["config"]["graph"] = False
+        line["config"]["weights"] = "expert tiles in pinned host memory, streamed host->device per layer"
+        line["host_stream"] = {"tiles_bytes_per_layer": tiles_bytes,
+                               "achieved_GBps": tiles_bytes * a.layers / sec_per_step / 1e9}
     print(json.dumps(line), flush=True)
     for ly in layers:
         ly.close()

@@ -139,6 +139,31 @@ typedef struct {
  * `stream`.  On success *out holds a handle for moe_destroy. */
 moe_status moe_create(const moe_desc* desc, const moe_weights* w, void* stream, moe_layer** out);
 
+/* moe_create with flags.  MOE_CREATE_HOST_TILES keeps the repacked expert
+ * tile images (the bulk of the layer, 11.3 GB for a DeepSeek-V3 layer) in
+ * pinned host memory instead of HBM: the Stream-Loading Prefill design of
+ * the CPU-GPU hybrid inference article (its "Stream-Loading Prefill"
+ * section: expert weights stay in CPU memory and stream into a GPU ring
+ * buffer while the previous experts compute), here over NVLink-C2C from
+ * Grace memory.  Such a layer runs only through moe_forward_tiles, on tiles
+ * that moe_tiles_load brought into a device slot; routing entries work as
+ * usual.  Scales, the router and the status word stay on the device. */
+#define MOE_CREATE_HOST_TILES 1u
+moe_status moe_create_ex(const moe_desc* desc, const moe_weights* w, uint32_t flags, void* stream, moe_layer** out);
+
+/* Bytes of the layer's tile images ([gate/up][down]) = the size of a slot. */
+moe_status moe_tiles_bytes(moe_layer* layer, size_t* bytes);
+
+/* Enqueue the copy of a host-tile layer's tiles into `slot` (device,
+ * 256-byte aligned, moe_tiles_bytes long) on `stream` (one copy-engine
+ * transfer; order it against the forward that reads the slot with events). */
+moe_status moe_tiles_load(moe_layer* layer, void* slot, void* stream);
+
+/* The forward of a host-tile layer on the tiles in `slot`.  mode, x, T, y,
+ * workspace and errors as for moe_forward_prefill / moe_forward_decode. */
+moe_status moe_forward_tiles(moe_layer* layer, int32_t mode, const void* slot, const uint16_t* x, int32_t T,
+                             uint16_t* y, void* ws, size_t ws_bytes, void* stream);
+
 /* Release everything the layer owns (synchronises the device first). */
 moe_status moe_destroy(moe_layer* layer);
 

@@ -23,10 +23,12 @@ __all__ = [
     "moe_route_from_logits_noalloc", "moe_forward_prefill", "moe_forward_decode", "moe_forward_host", "moe_get_device_status",
     "moe_set_wait_limit", "moe_debug_timeout_probe", "moe_profile_enable", "moe_profile_read", "moe_status_string", "moe_last_error",
     "moe_abi_version", "moe_forward_smallep", "moe_forward_deferred", "moe_layers_workspace_bytes",
-    "moe_forward_layers", "smallep_groups", "library_path", "load", "Layer", "LayerStackGraph",
+    "moe_forward_layers", "smallep_groups", "moe_create_ex", "moe_tiles_bytes", "moe_tiles_load", "moe_forward_tiles",
+    "CREATE_HOST_TILES", "library_path", "load", "Layer", "LayerStackGraph", "StreamedStack",
 ]
 
 MODE_ROUTE, MODE_PREFILL, MODE_DECODE = 0, 1, 2
+CREATE_HOST_TILES = 1
 DECODE_MAX_T = 64
 MOE_OK = 0
 DEV_BAD_EXPERT_ID, DEV_BAD_ROW, DEV_WAIT_TIMEOUT = 0x1, 0x2, 0x4
@@ -93,6 +95,10 @@ def load(build_if_missing: bool = False):
             "moe_debug_timeout_probe": ([vp, vp], st),
             "moe_route_from_logits_noalloc": ([vp, vp, i32, ctypes.POINTER(MoeRouteOut), vp], st),
             "moe_forward_smallep": ([vp, i32, i32, vp, i32, vp, vp, sz, vp], st),
+            "moe_create_ex": ([ctypes.POINTER(MoeDesc), ctypes.POINTER(MoeWeights), u32, vp, ctypes.POINTER(vp)], st),
+            "moe_tiles_bytes": ([vp, ctypes.POINTER(sz)], st),
+            "moe_tiles_load": ([vp, vp, vp], st),
+            "moe_forward_tiles": ([vp, i32, vp, vp, i32, vp, vp, sz, vp], st),
             "moe_forward_deferred": ([vp, i32, vp, i32, vp, vp, vp, vp, sz, vp], st),
             "moe_layers_workspace_bytes": ([ctypes.POINTER(vp), i32, i32, i32, ctypes.POINTER(sz)], st),
             "moe_forward_layers": ([ctypes.POINTER(vp), i32, i32, vp, i32, vp, vp, sz, vp], st),
@@ -142,6 +148,27 @@ def moe_create(desc: MoeDesc, weights: MoeWeights, stream: int = 0) -> int:
     h = ctypes.c_void_p()
     _check(load().moe_create(ctypes.byref(desc), ctypes.byref(weights), stream, ctypes.byref(h)))
     return h.value
+
+
+def moe_create_ex(desc: MoeDesc, weights: MoeWeights, flags: int, stream: int = 0) -> int:
+    h = ctypes.c_void_p()
+    _check(load().moe_create_ex(ctypes.byref(desc), ctypes.byref(weights), flags, stream, ctypes.byref(h)))
+    return h.value
+
+
+def moe_tiles_bytes(layer: int) -> int:
+    n = ctypes.c_size_t()
+    _check(load().moe_tiles_bytes(layer, ctypes.byref(n)))
+    return n.value
+
+
+def moe_tiles_load(layer: int, slot: int, stream: int = 0) -> None:
+    _check(load().moe_tiles_load(layer, slot, stream))
+
+
+def moe_forward_tiles(layer: int, mode: int, slot: int, x: int, T: int, y: int, ws: int, ws_bytes: int,
+                      stream: int = 0) -> None:
+    _check(load().moe_forward_tiles(layer, mode, slot, x, T, y, ws, ws_bytes, stream))
 
 
 def moe_destroy(layer: int) -> None:
@@ -254,7 +281,8 @@ class Layer:
     The library copies the weights; the tensors may be freed afterwards.
     """
 
-    def __init__(self, hidden, inter, n_experts, top_k, weights: dict, n_shared: int = 1, stream=None):
+    def __init__(self, hidden, inter, n_experts, top_k, weights: dict, n_shared: int = 1, stream=None,
+                 host_tiles: bool = False):
         import torch
         self.desc = MoeDesc(hidden, inter, n_experts, top_k, n_shared, inter if n_shared else 0)
         p = lambda n: (weights[n].data_ptr() if weights.get(n) is not None else None)
@@ -262,7 +290,7 @@ class Layer:
             p("router_w"), p("router_b"), p("w_gate"), p("w_up"), p("w_down"), p("s_gate"), p("s_up"), p("s_down"),
             p("sh_gate"), p("sh_up"), p("sh_down"), p("sh_s_gate"), p("sh_s_up"), p("sh_s_down"))
         self.stream = stream if stream is not None else torch.cuda.current_stream().cuda_stream
-        self.handle = moe_create(self.desc, self.weights, self.stream)
+        self.handle = moe_create_ex(self.desc, self.weights, CREATE_HOST_TILES if host_tiles else 0, self.stream)
         self._ws = {}
 
     def workspace(self, T: int, mode: int):
@@ -317,3 +345,49 @@ class LayerStackGraph:
     def replay(self):
         """Launch the captured stack on the current torch stream."""
         self.graph.replay()
+
+
+class StreamedStack:
+    """A stack of host-tile layers (moe_create_ex with CREATE_HOST_TILES) run
+    through a two-slot device ring: while layer l computes from slot l % 2,
+    a copy stream loads layer l + 1's tiles into the other slot (ordered by
+    events: a slot is reloaded only after the layer that read it finished).
+    x and y: torch CUDA [T][H] bf16-bits tensors; run() computes on the
+    current torch stream and returns when the work is enqueued."""
+
+    def __init__(self, layers, mode: int, x, y):
+        import torch
+        self.layers = list(layers)
+        self.mode, self.x, self.y = mode, x, y
+        T = x.shape[0]
+        slot_bytes = max(moe_tiles_bytes(ly.handle) for ly in self.layers)
+        self.slots = [torch.empty(slot_bytes, dtype=torch.uint8, device=x.device) for _ in range(2)]
+        self.acts = [torch.empty_like(x) for _ in range(2)]
+        need = max(moe_workspace_bytes(ly.handle, T, mode) for ly in self.layers)
+        self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+        self.copy = torch.cuda.Stream(device=x.device)
+        self.loaded = [torch.cuda.Event() for _ in range(2)]
+        self.done = [torch.cuda.Event() for _ in range(2)]
+
+    def run(self):
+        import torch
+        comp = torch.cuda.current_stream()
+        n, T = len(self.layers), self.x.shape[0]
+
+        def load_into(l):
+            s = l % 2
+            self.copy.wait_event(self.done[s]) if l >= 2 else self.copy.wait_stream(comp)
+            moe_tiles_load(self.layers[l].handle, self.slots[s].data_ptr(), self.copy.cuda_stream)
+            self.loaded[s].record(self.copy)
+
+        load_into(0)
+        for l in range(n):
+            if l + 1 < n:
+                load_into(l + 1)
+            s = l % 2
+            comp.wait_event(self.loaded[s])
+            src = self.x if l == 0 else self.acts[(l - 1) % 2]
+            dst = self.y if l == n - 1 else self.acts[l % 2]
+            moe_forward_tiles(self.layers[l].handle, self.mode, self.slots[s].data_ptr(), src.data_ptr(), T,
+                              dst.data_ptr(), self.ws.data_ptr(), self.ws.numel(), comp.cuda_stream)
+            self.done[s].record(comp)

@@ -84,6 +84,8 @@ moe_status check_layer(const moe_layer* L) {
 moe_status check_call(moe_layer* L, int T, int mode, const void* x, const void* y, void* ws, size_t ws_bytes,
                       moe::WsLayout* lay) {
     moe_status st = check_layer(L);
+    if (st == MOE_OK && mode != MOE_MODE_ROUTE && L->tiles_host && !L->w_gu)
+        return fail(MOE_ERR_INVALID_ARG, "the layer keeps its tiles in host memory: run it with moe_forward_tiles");
     if (st != MOE_OK) return st;
     if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T = %d is negative", T);
     if ((int64_t)T * L->d.top_k >= (int64_t)1 << 31) return fail(MOE_ERR_UNSUPPORTED, "T * top_k >= 2^31");
@@ -204,7 +206,13 @@ MOE_EXPORT const char* moe_status_string(moe_status s) {
 }
 
 MOE_EXPORT moe_status moe_create(const moe_desc* d, const moe_weights* w, void* stream, moe_layer** out) {
+    return moe_create_ex(d, w, 0, stream, out);
+}
+
+MOE_EXPORT moe_status moe_create_ex(const moe_desc* d, const moe_weights* w, uint32_t flags, void* stream,
+                                    moe_layer** out) {
     g_last_error.clear();
+    if (flags & ~(uint32_t)MOE_CREATE_HOST_TILES) return fail(MOE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
     if (!d || !w || !out) return fail(MOE_ERR_INVALID_ARG, "desc, weights and out must be non-NULL");
     *out = nullptr;
     if (d->hidden <= 0 || d->inter <= 0 || d->hidden % moe::QB || d->inter % moe::QB)
@@ -245,6 +253,8 @@ MOE_EXPORT moe_status moe_create(const moe_desc* d, const moe_weights* w, void* 
     const size_t H = d->hidden, I = d->inter, E = d->n_experts, G = E + L->d.n_shared;
     L->n_groups_max = (int)G;
     const size_t gu = G * I * H * 2, dn = G * H * I;
+    L->gu_bytes = gu;
+    L->dn_bytes = dn;
     const size_t sgu = G * (I / moe::QB) * (H / moe::QB) * 2 * 4, sdn = G * (H / moe::QB) * (I / moe::QB) * 4;
     if ((e = cudaMalloc(&L->w_gu, gu)) != cudaSuccess) return cleanup(cuda_fail(e, "allocating gate/up tiles"));
     if ((e = cudaMalloc(&L->w_dn, dn)) != cudaSuccess) return cleanup(cuda_fail(e, "allocating down tiles"));
@@ -268,8 +278,56 @@ MOE_EXPORT moe_status moe_create(const moe_desc* d, const moe_weights* w, void* 
     if ((e = moe::launch_repack(L, w, s)) != cudaSuccess) return cleanup(cuda_fail(e, "weight repack"));
     if ((e = moe::launch_tc_scale_records(L, s)) != cudaSuccess) return cleanup(cuda_fail(e, "scale records"));
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cleanup(cuda_fail(e, "moe_create synchronise"));
+    if (flags & MOE_CREATE_HOST_TILES) {
+        // keep the tile images in pinned host memory, [gate/up][down]; the device copies are released
+        if ((e = cudaHostAlloc(&L->tiles_host, gu + dn, cudaHostAllocDefault)) != cudaSuccess)
+            return cleanup(cuda_fail(e, "allocating host tiles"));
+        if ((e = cudaMemcpy(L->tiles_host, L->w_gu, gu, cudaMemcpyDeviceToHost)) != cudaSuccess ||
+            (e = cudaMemcpy(L->tiles_host + gu, L->w_dn, dn, cudaMemcpyDeviceToHost)) != cudaSuccess) {
+            cudaFreeHost(L->tiles_host);
+            L->tiles_host = nullptr;
+            return cleanup(cuda_fail(e, "copying tiles to host"));
+        }
+        cudaFree(L->w_gu);
+        cudaFree(L->w_dn);
+        L->w_gu = L->w_dn = nullptr;
+    }
     *out = L;
     return MOE_OK;
+}
+
+MOE_EXPORT moe_status moe_tiles_bytes(moe_layer* L, size_t* bytes) {
+    moe_status st = check_layer(L);
+    if (st != MOE_OK) return st;
+    if (!bytes) return fail(MOE_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = L->gu_bytes + L->dn_bytes;
+    return MOE_OK;
+}
+
+MOE_EXPORT moe_status moe_tiles_load(moe_layer* L, void* slot, void* stream) {
+    moe_status st = check_layer(L);
+    if (st != MOE_OK) return st;
+    if (!L->tiles_host) return fail(MOE_ERR_INVALID_ARG, "the layer keeps its tiles on the device");
+    if (!slot || !aligned(slot, 256)) return fail(MOE_ERR_INVALID_ARG, "slot NULL or not 256-byte aligned");
+    MOE_CUDA(cudaMemcpyAsync(slot, L->tiles_host, L->gu_bytes + L->dn_bytes, cudaMemcpyHostToDevice,
+                             static_cast<cudaStream_t>(stream)),
+             "loading tiles");
+    return MOE_OK;
+}
+
+MOE_EXPORT moe_status moe_forward_tiles(moe_layer* L, int32_t mode, const void* slot, const uint16_t* x, int32_t T,
+                                        uint16_t* y, void* ws, size_t ws_bytes, void* stream) {
+    moe_status st = check_layer(L);
+    if (st != MOE_OK) return st;
+    if (mode != MOE_MODE_PREFILL && mode != MOE_MODE_DECODE) return fail(MOE_ERR_INVALID_ARG, "mode must be 1 or 2");
+    if (!L->tiles_host) return fail(MOE_ERR_INVALID_ARG, "the layer keeps its tiles on the device");
+    if (!slot || !aligned(slot, 256)) return fail(MOE_ERR_INVALID_ARG, "slot NULL or not 256-byte aligned");
+    // the kernels take the tile pointers by value at launch; the handle is used from one stream at a time
+    L->w_gu = static_cast<uint8_t*>(const_cast<void*>(slot));
+    L->w_dn = L->w_gu + L->gu_bytes;
+    st = run_forward(L, mode, x, T, y, nullptr, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+    L->w_gu = L->w_dn = nullptr;
+    return st;
 }
 
 MOE_EXPORT moe_status moe_destroy(moe_layer* L) {
@@ -277,6 +335,7 @@ MOE_EXPORT moe_status moe_destroy(moe_layer* L) {
     cudaError_t e = cudaDeviceSynchronize();
     if (L->profile)
         for (cudaEvent_t ev : L->ev) cudaEventDestroy(ev);
+    if (L->tiles_host) cudaFreeHost(L->tiles_host);
     cudaFree(L->w_gu); cudaFree(L->w_dn); cudaFree(L->s_gu); cudaFree(L->s_dn); cudaFree(L->r_gu); cudaFree(L->r_dn);
     cudaFree(L->router_w); cudaFree(L->router_w3); cudaFree(L->router_b); cudaFree(L->dev_status);
     delete L;

@@ -147,6 +147,9 @@ struct moe_layer {
     int n_groups_max;      // E + n_shared
     uint8_t* w_gu;         // [G][I/128][H/128][2][16 KB] gate/up tile images
     uint8_t* w_dn;         // [G][H/128][I/128][16 KB]    down tile images
+    uint8_t* tiles_host;   // host-resident tiles ([gate/up][down], pinned) or NULL; then w_gu / w_dn
+                           // point into a device slot only for the duration of moe_forward_tiles
+    size_t gu_bytes, dn_bytes;
     float* s_gu;           // [G][I/128][H/128][2]
     float* s_dn;           // [G][H/128][I/128]
     float* r_gu;           // [G][I/128][H/128][4]: {gate, up, 0, 0} per k block (16-byte records)

@@ -19,9 +19,9 @@ def to_dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-def make_layer(wl: synth.Workload, inp: dict) -> moe.Layer:
+def make_layer(wl: synth.Workload, inp: dict, host_tiles: bool = False) -> moe.Layer:
     dev = {k: to_dev(inp.get(k)) for k in WEIGHT_KEYS}
-    layer = moe.Layer(wl.hidden, wl.inter, wl.n_experts, wl.top_k, dev, n_shared=wl.n_shared)
+    layer = moe.Layer(wl.hidden, wl.inter, wl.n_experts, wl.top_k, dev, n_shared=wl.n_shared, host_tiles=host_tiles)
     del dev
     return layer
 

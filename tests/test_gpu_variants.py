@@ -11,6 +11,9 @@
   within the layer tolerance.
 - moe_forward_deferred: deferred slots split off into y_next (lecture section
   4.3, expert deferral); checked against the oracle's fp64 partial sums.
+- Host-tile layers (moe_create_ex with MOE_CREATE_HOST_TILES) run through the
+  two-slot ring of StreamedStack (the hybrid-inference article's
+  Stream-Loading Prefill): must equal the same layers kept in HBM, bit for bit.
 """
 import numpy as np
 import pytest
@@ -197,3 +200,42 @@ def test_deferral_split(h, mode, T):
     close(now, y_keep, "y_now")
     close(nxt, y_def - y_sh, "y_next")
     layer.close()
+
+
+# ------------------------------------------------------------------ host tiles, two-slot ring
+
+@pytest.mark.parametrize("mode,T", [(1, 200), (2, 16)])
+def test_streamed_stack_equals_resident(h, mode, T):
+    import moe_expert_ffn_02_gb300 as moe
+    wl = small_wl(8, 2, T=T)
+    inps = [synth.make_inputs(wl, seed=s) for s in (11, 12, 13)]
+    resident = [h.make_layer(wl, inp) for inp in inps]
+    hosted = [h.make_layer(wl, inp, host_tiles=True) for inp in inps]
+    x0 = dev(inps[0]["x"].view(np.int16))
+
+    y_ref = torch.empty_like(x0)
+    handles = [ly.handle for ly in resident]
+    need = moe.moe_layers_workspace_bytes(handles, T, mode)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    moe.moe_forward_layers(handles, mode, x0.data_ptr(), T, y_ref.data_ptr(), ws.data_ptr(), need,
+                           torch.cuda.current_stream().cuda_stream)
+
+    y = torch.empty_like(x0)
+    ring = moe.StreamedStack(hosted, mode, x0, y)
+    for _ in range(2):                                  # a second pass reuses both slots
+        y.zero_()
+        ring.run()
+        torch.cuda.synchronize()
+        assert np.array_equal(y.cpu().numpy(), y_ref.cpu().numpy())
+    for ly in hosted:
+        assert moe.moe_get_device_status(ly.handle, 0) == (0, 0)
+
+    # a host-tile layer needs a slot; a resident layer has nothing to load
+    ws1, nb1 = hosted[0].workspace(T, mode)
+    with pytest.raises(moe.MoeError):
+        moe.moe_forward_prefill(hosted[0].handle, x0.data_ptr(), T, y.data_ptr(), None, ws1, nb1, 0)
+    with pytest.raises(moe.MoeError):
+        moe.moe_tiles_load(resident[0].handle, ring.slots[0].data_ptr(), 0)
+    assert moe.moe_tiles_bytes(hosted[0].handle) == moe.moe_tiles_bytes(resident[0].handle)
+    for ly in resident + hosted:
+        ly.close()
