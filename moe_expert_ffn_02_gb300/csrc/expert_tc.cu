@@ -19,10 +19,11 @@
 // per-thread scalar and the weight scales s_w[kb] are uniform; the epilogue
 // warps read each block's partial with tcgen05.ld and promote it with fp32
 // FMAs into registers (scalar FFMA on the loaded registers: packing them into
-// pairs for fma.rn.f32x2 costs more moves than it saves).  Both scales ride in the stage with the
-// operands (two more bulk copies), so the epilogue reads them from shared
-// memory; a stage is free again once the MMAs that read it have completed
-// and all epilogue warps have taken their scales.  Gate/up then forms h = SiLU(g)*u and its
+// pairs for fma.rn.f32x2 costs more moves than it saves).  Both scales are
+// copied with the stage's operands into a scale ring of their own, so the
+// epilogue reads them from shared memory; a stage is free again once the
+// MMAs that read it have completed, a scale slot once every epilogue warp
+// has taken its scales.  Gate/up then forms h = SiLU(g)*u and its
 // 1x128 E4M3 codes (the activation and elementwise product between gate/up
 // and down, "CPU fine-grained parallelism" section of the same article);
 // down writes fp32 output rows.
@@ -50,12 +51,17 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr int STAGES = 4;
 constexpr int W_BYTES = 2 * TILE_BYTES;   // 256 weight rows
 constexpr int X_BYTES = BM * 128;         // 128 token rows
-// Stage tail: the 128 tokens' activation scales of this k block (512 B)
-// and the weight-scale record (16 B), padded so the next stage's operand
-// images stay 1024-byte aligned.
+constexpr int STAGE = W_BYTES + X_BYTES;
+// Scale ring: per k block the 128 tokens' activation scales (512 B) and the
+// weight-scale record (16 B), in SSLOTS slots of their own.  They are copied
+// with the stage (counted on its full barrier), but a stage is free as soon
+// as its MMAs complete, while a scale slot is freed by the epilogue warps
+// once they have read it.
 constexpr int S_BYTES = BM * 4;
 constexpr int R_BYTES = 16;
-constexpr int STAGE = W_BYTES + X_BYTES + 1024;
+constexpr int SSLOTS = 8;
+constexpr int SSLOT = S_BYTES + R_BYTES;
+static_assert(SSLOTS >= STAGES + 2, "a scale slot must outlive its stage and both TMEM buffers");
 // + amax exchange + the group table copy (units are decoded from shared
 // memory; up to 385 groups, larger tables are read in place) + the down
 // epilogue's per-warp staging tiles (32 rows x 16 floats, rows 20 floats
@@ -63,7 +69,7 @@ constexpr int STAGE = W_BYTES + X_BYTES + 1024;
 constexpr int GT_SMEM_CAP = 386;
 constexpr int STG_STRIDE = 20;
 constexpr int STG_BYTES = EPI_WARPS * 32 * STG_STRIDE * 4;
-constexpr int SMEM = STAGES * STAGE + 2 * 4 * 32 * 4 + gt_smem_bytes(GT_SMEM_CAP) + STG_BYTES + 256;
+constexpr int SMEM = STAGES * STAGE + SSLOTS * SSLOT + 2 * 4 * 32 * 4 + gt_smem_bytes(GT_SMEM_CAP) + STG_BYTES + 256;
 // dynamic (with 1024 bytes of alignment slack) + static (barriers, padded to 1024) <= 227 KB
 static_assert(SMEM + 1024 + 1024 <= 232448, "shared memory budget");
 
@@ -110,10 +116,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
-    float* amax_x = reinterpret_cast<float*>(smem + STAGES * STAGE);   // [2 halves][4 quarters][32 lanes]
-    int* gt_s = reinterpret_cast<int*>(smem + STAGES * STAGE + 2 * 4 * 32 * 4);
-    float* stg_all = reinterpret_cast<float*>(smem + STAGES * STAGE + 2 * 4 * 32 * 4 + gt_smem_bytes(GT_SMEM_CAP));
-    __shared__ uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2];
+    uint8_t* sring = smem + STAGES * STAGE;                                 // [SSLOTS][SSLOT]
+    uint8_t* after = sring + SSLOTS * SSLOT;
+    float* amax_x = reinterpret_cast<float*>(after);                       // [2 halves][4 quarters][32 lanes]
+    int* gt_s = reinterpret_cast<int*>(after + 2 * 4 * 32 * 4);
+    float* stg_all = reinterpret_cast<float*>(after + 2 * 4 * 32 * 4 + gt_smem_bytes(GT_SMEM_CAP));
+    __shared__ uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], sempty[SSLOTS];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -126,7 +134,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
     const SGroups sg = load_groups(gt, gt_s, threadIdx.x, NTHREADS, GT_SMEM_CAP);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1 + EPI_WARPS); }
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        for (int s = 0; s < SSLOTS; ++s) mbar_init(&sempty[s], EPI_WARPS);
         for (int b = 0; b < 2; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], EPI_WARPS); }
         fence_mbar_init();
         abort_flag = 0;
@@ -142,8 +151,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CTRL_REGS));
         if (warp == 0 && lane == 0) {
             // -------------------------------------------------------- producer
-            int stage = 0;
-            uint32_t phase = 0, armed = 0, armed_par = 0;
+            int stage = 0, slot = 0;
+            uint32_t phase = 0, sphase = 0, armed = 0, armed_par = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
                 const Unit un = decode_unit(sg, u, NB);
@@ -154,11 +163,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
                 const uint32_t wbytes = two ? (uint32_t)W_BYTES : (uint32_t)TILE_BYTES;
                 const uint8_t* wbase = a.w + ((size_t)(un.expert * MT128 + t0) * KT) * (GU ? W_BYTES : TILE_BYTES);
                 for (int kb = 0; kb < KT; ++kb) {
-                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, a.wait_limit, a.status, abort)) {
+                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, a.wait_limit, a.status, abort) ||
+                        !mbar_wait_bounded(&sempty[slot], sphase ^ 1u, a.wait_limit, a.status, abort)) {
                         ok = false;
                         break;
                     }
                     uint8_t* st = stages + stage * STAGE;
+                    uint8_t* ss = sring + slot * SSLOT;
                     mbar_arrive_expect_tx(&full[stage], wbytes + X_BYTES + S_BYTES + R_BYTES);
                     if (GU) {
                         bulk_g2s(st, wbase + (size_t)kb * W_BYTES, W_BYTES, &full[stage]);
@@ -168,12 +179,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
                             bulk_g2s(st + TILE_BYTES, wbase + ((size_t)KT + kb) * TILE_BYTES, TILE_BYTES, &full[stage]);
                     }
                     bulk_g2s(st + W_BYTES, a.act + act_offset(kb, un.row_begin, a.ld), X_BYTES, &full[stage]);
-                    bulk_g2s(st + W_BYTES + X_BYTES, a.actsT + (size_t)kb * a.ld + un.row_begin, S_BYTES, &full[stage]);
-                    bulk_g2s(st + W_BYTES + X_BYTES + S_BYTES, a.wrec + (((size_t)un.expert * NB + un.wb) * KT + kb) * 4,
-                             R_BYTES, &full[stage]);
+                    bulk_g2s(ss, a.actsT + (size_t)kb * a.ld + un.row_begin, S_BYTES, &full[stage]);
+                    bulk_g2s(ss + S_BYTES, a.wrec + (((size_t)un.expert * NB + un.wb) * KT + kb) * 4, R_BYTES,
+                             &full[stage]);
                     armed |= 1u << stage;
                     armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    if (++slot == SSLOTS) { slot = 0; sphase ^= 1u; }
                 }
             }
             for (int s = 0; s < STAGES; ++s)
@@ -217,7 +229,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
         const int quarter = warp & 3;               // TMEM lanes this warp may read
         const int half = ew >> 2;                   // column half of the 256-column buffer
         const int r = quarter * 32 + lane;          // token row inside the tile
-        int buf = 0, stage = 0;
+        int buf = 0, slot = 0;
         uint32_t tphase = 0;
         bool dead = false;
         for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
@@ -235,8 +247,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
                 if (!dead && !mbar_wait_bounded(&tfull[buf], tphase, a.wait_limit, a.status, abort)) dead = true;
                 if (!dead) {
                     tc_fence_after();
-                    // this block's scales from the stage tail: s_x of my token, the record's weight scales
-                    const uint8_t* tail = stages + stage * STAGE + W_BYTES + X_BYTES;
+                    // this block's scales from its scale slot: s_x of my token, the record's weight scales
+                    const uint8_t* tail = sring + slot * SSLOT;
                     const float sx = reinterpret_cast<const float*>(tail)[r];
                     const float2 sw = *reinterpret_cast<const float2*>(tail + S_BYTES);
                     const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN);
@@ -254,7 +266,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
                     const float c0 = (GU || half == 0) ? sw.x * sx : sw.y * sx;
                     const float c1 = sw.y * sx;
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[stage]);
+                    if (lane == 0) mbar_arrive(&sempty[slot]);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -268,14 +280,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
                         if (i < 3) tmem_wait_ld();
                     }
                     tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty[buf]);
                 } else {
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[stage]);
+                    if (lane == 0) {
+                        mbar_arrive(&sempty[slot]);
+                        mbar_arrive(&tempty[buf]);
+                    }
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[buf]);
                 if (++buf == 2) { buf = 0; tphase ^= 1u; }
-                if (++stage == STAGES) stage = 0;
+                if (++slot == SSLOTS) slot = 0;
             }
 
             if (GU) {
