@@ -59,6 +59,7 @@ def parse():
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-graph", action="store_true", help="decode: time plain launches instead of a graph replay")
     p.add_argument("--layers", type=int, default=1,
                    help="> 1: time a stack of this many layers (distinct weight copies in HBM, distinct routers), "
                         "captured as one CUDA graph; the metric is then per layer")
@@ -275,7 +276,17 @@ def run_ours(a, wl):
         flush.zero_()
         step()
     torch.cuda.synchronize()
+    # per-stage events of the library (for the dominant kernel's roofline), recorded in every timed step
     moe.moe_profile_enable(layer.handle, True)
+    # decode: the step is one CUDA graph replay (the layer's kernels, and the stage events, captured once),
+    # as a decode loop runs it
+    graph = None
+    if mode == moe.MODE_DECODE and not a.no_graph:
+        graph = moe.LayerStackGraph([layer.handle], mode, x, y)
+        for _ in range(a.warmup):
+            flush.zero_()
+            graph.replay()
+        torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
     stage_ms = []
@@ -287,7 +298,7 @@ def run_ours(a, wl):
         for i in range(a.steps):
             flush.zero_()
             starts[i].record(stream)
-            step()
+            graph.replay() if graph is not None else step()
             ends[i].record(stream)
             stage_ms.append(moe.moe_profile_read(layer.handle))
         torch.cuda.synchronize()
@@ -383,6 +394,7 @@ def run_ours(a, wl):
             "dtype": "fp8_e4m3", "data": "synthetic",
             "config": {"workload": wl.name, "T": T, "hidden": H, "inter": wl.inter, "n_experts": wl.n_experts,
                        "top_k": wl.top_k, "n_shared": wl.n_shared, "parallelism": f"replicas{world}",
+                       "graph": graph is not None,
                        "l2": "flushed between steps (512 MiB write, outside the timed events)"},
             "roofline": roof, "layer_roofline": layer_roof, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": n_launches * world,

@@ -155,7 +155,12 @@ moe_status run_forward(moe_layer* L, int mode, const uint16_t* x, int T, uint16_
     auto mark = [&](int i) -> cudaError_t {
         if (!L->profile) return cudaSuccess;
         L->ev_stream = s;
-        return cudaEventRecord(L->ev[i], s);
+        // inside a stream capture the events become record nodes of the graph (recorded at each launch)
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        cudaError_t e = cudaStreamIsCapturing(s, &cap);
+        if (e != cudaSuccess) return e;
+        return cap == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(L->ev[i], s, cudaEventRecordExternal)
+                                                    : cudaEventRecord(L->ev[i], s);
     };
     // prefill: tcgen05 grouped GEMMs (128-token tiles); decode: weight-streaming kernels (64-token tiles)
     const bool tc_path = (mode == MOE_MODE_PREFILL);

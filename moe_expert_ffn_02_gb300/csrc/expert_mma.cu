@@ -37,6 +37,7 @@ constexpr int BN = 64;                  // rows (tokens) per n tile
 constexpr int CW = 8;                   // consumer warps (16 output rows each)
 constexpr int NTHREADS = (CW + 1) * 32; // + producer warp
 constexpr int XSTRIDE = 128;            // activation row in shared memory (swizzled)
+constexpr int GT_CAP_DEC = 386;         // groups held in the shared-memory table copy (+1)
 
 // Stage tail: the tile rows' activation scales of this k block (BN floats)
 // and the 16-byte weight-scale record, brought by the producer with the
@@ -50,9 +51,10 @@ struct Cfg {
     static constexpr int W_BYTES = GU ? 2 * TILE_BYTES : TILE_BYTES;
     static constexpr int X_BYTES = BN * XSTRIDE;
     static constexpr int STAGE = W_BYTES + X_BYTES + TAIL;
-    static constexpr int STAGES = GU ? 4 : 6;
+    static constexpr int STAGES = GU ? 5 : 7;           // as deep as shared memory allows (HBM latency)
     static constexpr int EPI = GU ? (BN * 144 + CW * BN * 4) : (BN * 132 * 4);
-    static constexpr int SMEM = STAGES * STAGE + EPI + GT_SMEM_BYTES + 2 * STAGES * 8 + 128;
+    // + the group table copy for up to 385 groups (larger tables are read in place)
+    static constexpr int SMEM = STAGES * STAGE + EPI + gt_smem_bytes(GT_CAP_DEC) + 2 * STAGES * 8 + 128;
 };
 
 struct ExpertArgs {
@@ -91,7 +93,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_gemm_kernel(ExpertArgs a) 
     uint8_t* stages = smem;
     uint8_t* epi = smem + C::STAGES * C::STAGE;
     int* gt_s = reinterpret_cast<int*>(epi + C::EPI);
-    uint64_t* full = reinterpret_cast<uint64_t*>(epi + C::EPI + GT_SMEM_BYTES);
+    uint64_t* full = reinterpret_cast<uint64_t*>(epi + C::EPI + gt_smem_bytes(GT_CAP_DEC));
     uint64_t* empty = full + C::STAGES;
     __shared__ int abort_flag;
 
@@ -99,7 +101,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_gemm_kernel(ExpertArgs a) 
     const int MT = a.M / QB, KT = a.K / QB;
     const GroupTable* gt = a.gt;
     const int n_units = gt->n_pairs * MT;
-    const SGroups sg = load_groups(gt, gt_s, threadIdx.x, NTHREADS);
+    const SGroups sg = load_groups(gt, gt_s, threadIdx.x, NTHREADS, GT_CAP_DEC);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
