@@ -81,6 +81,15 @@ def test_tiny_layer_parity(h, mode):
     check_layer(h, wl, synth.make_inputs(wl, seed=0), mode)
 
 
+@pytest.mark.parametrize("mode,T,k", [(1, 400, 8), (2, 64, 16)])
+def test_many_experts_group_table_in_place(h, mode, T, k):
+    """512 routed experts + shared, ~450-510 of them touched: more groups than
+    the expert GEMMs copy into shared memory (385), so they decode their units
+    from the table in place."""
+    wl = small_wl(512, k, H=256, I=256, T=T)
+    check_layer(h, wl, synth.make_inputs(wl, seed=8), mode)
+
+
 @pytest.mark.parametrize("T", [1, 3, 17, 64])
 def test_decode_entry_small_batches(h, T):
     wl = small_wl(16, 4, H=384, I=256, T=T)
