@@ -112,6 +112,26 @@ moe_status run_route(moe_layer* L, const uint16_t* x, const float* logits_in, in
     const int k = L->d.top_k;
     int32_t* ids = reinterpret_cast<int32_t*>(ws + lay.ids);
     float* w = reinterpret_cast<float*>(ws + lay.w);
+    // a decode-sized batch: top-k and grouping in one single-CTA kernel
+    const bool small = lay.n_chunks == 1 && L->d.n_experts <= 512;
+    if (small) {
+        const float* part = logits_in ? logits_in : reinterpret_cast<const float*>(ws + lay.logit_part);
+        if (!logits_in)
+            MOE_CUDA(moe::launch_router_logits(L, x, T, const_cast<float*>(part), lay.ksplit, lay.gemv, s),
+                     "router logits");
+        MOE_CUDA(moe::launch_route_small(L, part, logits_in ? 1 : lay.ksplit, !logits_in, T,
+                                         (dbg && !logits_in) ? dbg->logits : nullptr, ids, w, lay, ws, bn,
+                                         dbg ? dbg->expert_offsets : nullptr, dbg ? dbg->sorted_token : nullptr,
+                                         dbg ? dbg->inv_row : nullptr, s),
+                 "routing");
+        if (dbg && dbg->topk_ids)
+            MOE_CUDA(cudaMemcpyAsync(dbg->topk_ids, ids, sizeof(int32_t) * (size_t)T * k, cudaMemcpyDeviceToDevice, s),
+                     "copy ids");
+        if (dbg && dbg->topk_w)
+            MOE_CUDA(cudaMemcpyAsync(dbg->topk_w, w, sizeof(float) * (size_t)T * k, cudaMemcpyDeviceToDevice, s),
+                     "copy weights");
+        return MOE_OK;
+    }
     if (logits_in) {
         MOE_CUDA(moe::launch_topk(L, logits_in, 1, false, T, nullptr, ids, w, s), "top-k");
     } else {

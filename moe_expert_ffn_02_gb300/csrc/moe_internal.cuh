@@ -309,6 +309,9 @@ cudaError_t launch_router_logits(const moe_layer* L, const uint16_t* x, int T, f
                                  cudaStream_t s);
 cudaError_t launch_topk(const moe_layer* L, const float* part, int ksplit, bool add_bias, int T, float* logits_out,
                         int32_t* ids, float* w, cudaStream_t s);
+cudaError_t launch_route_small(const moe_layer* L, const float* part, int ksplit, bool add_bias, int T,
+                               float* logits_out, int32_t* ids, float* w, const WsLayout& lay, char* ws, int bn,
+                               int32_t* offsets_out, int32_t* sorted_out, int32_t* inv_out, cudaStream_t s);
 cudaError_t launch_permute(const moe_layer* L, const int32_t* ids, int T, const WsLayout& lay, char* ws, int bn,
                            int32_t* offsets_out, int32_t* sorted_out, int32_t* inv_out, cudaStream_t s);
 cudaError_t launch_quant_scatter(const moe_layer* L, const uint16_t* x, int T, const WsLayout& lay, char* ws,

@@ -156,15 +156,9 @@ __device__ __forceinline__ float gate_exp(float x) {
 // left to right; w_j = e_j / S -- each step an IEEE-rounded fp32 op.
 // ---------------------------------------------------------------------------
 template <int PER>
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ part, int ksplit,
-                                                   const float* __restrict__ bias, int T, int E, int k,
-                                                   float* __restrict__ logits_out, int32_t* __restrict__ ids,
-                                                   float* __restrict__ wout) {
-    __shared__ float sel_v[8][MAX_TOPK];
-    __shared__ int sel_i[8][MAX_TOPK];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 8 + warp;
-    if (t >= T) return;
+__device__ void topk_token(const float* __restrict__ part, int ksplit, const float* __restrict__ bias, int T, int E,
+                           int k, float* __restrict__ logits_out, int32_t* __restrict__ ids,
+                           float* __restrict__ wout, int t, int lane, float* sel_v, int* sel_i) {
     // logits: the ksplit partial sums added in split order, then the bias.  The
     // partials are fetched ZB splits at a time for all PER experts of the lane
     // before any addition, so the loads are in flight together.
@@ -217,22 +211,36 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
             if (better) { bv = ov; bi = oi; }
         }
         if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        if (lane == 0) { sel_v[warp][j] = bv; sel_i[warp][j] = bi; }
+        if (lane == 0) { sel_v[j] = bv; sel_i[j] = bi; }
     }
     __syncwarp();
     if (lane == 0) {
-        const float m = sel_v[warp][0];
+        const float m = sel_v[0];
         float ev[MAX_TOPK];
         float S = 0.0f;
         for (int j = 0; j < k; ++j) {
-            ev[j] = gate_exp(__fsub_rn(sel_v[warp][j], m));
+            ev[j] = gate_exp(__fsub_rn(sel_v[j], m));
             S = (j == 0) ? ev[0] : __fadd_rn(S, ev[j]);
         }
         for (int j = 0; j < k; ++j) {
-            if (ids) ids[(size_t)t * k + j] = sel_i[warp][j];
+            if (ids) ids[(size_t)t * k + j] = sel_i[j];
             if (wout) wout[(size_t)t * k + j] = __fdiv_rn(ev[j], S);
         }
     }
+    __syncwarp();
+}
+
+template <int PER>
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ part, int ksplit,
+                                                   const float* __restrict__ bias, int T, int E, int k,
+                                                   float* __restrict__ logits_out, int32_t* __restrict__ ids,
+                                                   float* __restrict__ wout) {
+    __shared__ float sel_v[8][MAX_TOPK];
+    __shared__ int sel_i[8][MAX_TOPK];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= T) return;
+    topk_token<PER>(part, ksplit, bias, T, E, k, logits_out, ids, wout, t, lane, sel_v[warp], sel_i[warp]);
 }
 
 cudaError_t launch_topk(const moe_layer* L, const float* part, int ksplit, bool add_bias, int T, float* logits_out,
@@ -276,14 +284,9 @@ __device__ __forceinline__ int clamp_expert(int e, int E, uint32_t* status) {
     return e;
 }
 
-__global__ void __launch_bounds__(128) perm_count_kernel(const int32_t* __restrict__ ids, int T, int E, int k,
-                                                         int n_chunks, int32_t* __restrict__ chunk_cnt,
-                                                         uint32_t* status) {
-    extern __shared__ int32_t cnt_smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int c = blockIdx.x * 4 + warp;
-    if (c >= n_chunks) return;
-    int32_t* cnt = cnt_smem + warp * E;
+// One warp counts chunk c (CHUNK_TOK tokens) into cnt (E ints of shared memory).
+__device__ void count_chunk(const int32_t* __restrict__ ids, int T, int E, int k, int c, int32_t* cnt,
+                            int32_t* __restrict__ chunk_cnt, uint32_t* status, int lane) {
     for (int e = lane; e < E; e += 32) cnt[e] = 0;
     __syncwarp();
     const int t0 = c * CHUNK_TOK;
@@ -297,11 +300,21 @@ __global__ void __launch_bounds__(128) perm_count_kernel(const int32_t* __restri
     for (int e = lane; e < E; e += 32) chunk_cnt[(size_t)c * E + e] = cnt[e];
 }
 
-// Exclusive scan across a 1024-thread block; returns this thread's prefix
-// and writes the block total to *total.
+__global__ void __launch_bounds__(128) perm_count_kernel(const int32_t* __restrict__ ids, int T, int E, int k,
+                                                         int n_chunks, int32_t* __restrict__ chunk_cnt,
+                                                         uint32_t* status) {
+    extern __shared__ int32_t cnt_smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x * 4 + warp;
+    if (c >= n_chunks) return;
+    count_chunk(ids, T, E, k, c, cnt_smem + warp * E, chunk_cnt, status, lane);
+}
+
+// Exclusive scan across the block (blockDim.x a multiple of 32, at most
+// 1024); returns this thread's prefix and writes the block total to *total.
 __device__ int block_excl_scan_1024(int v, int* total) {
     __shared__ int warp_sums[32];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     int incl = v;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -311,7 +324,7 @@ __device__ int block_excl_scan_1024(int v, int* total) {
     if (lane == 31) warp_sums[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        const int ws = warp_sums[lane];
+        const int ws = lane < nwarps ? warp_sums[lane] : 0;
         int wi = ws;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -327,12 +340,11 @@ __device__ int block_excl_scan_1024(int v, int* total) {
     return r;
 }
 
-__global__ void __launch_bounds__(1024) perm_scan_kernel(const int32_t* __restrict__ chunk_cnt, int n_chunks, int T,
-                                                         int E, int k, int n_shared, int bn,
-                                                         int32_t* __restrict__ chunk_base,
-                                                         int32_t* __restrict__ offsets,
-                                                         int32_t* __restrict__ offsets_pad,
-                                                         int32_t* __restrict__ offsets_out, GroupTable* gt) {
+// Offsets, padded offsets and the group table from the chunk counts; thread e
+// of the block handles expert e (blockDim.x >= E).
+__device__ void scan_groups(const int32_t* __restrict__ chunk_cnt, int n_chunks, int T, int E, int k, int n_shared,
+                            int bn, int32_t* __restrict__ chunk_base, int32_t* __restrict__ offsets,
+                            int32_t* __restrict__ offsets_pad, int32_t* __restrict__ offsets_out, GroupTable* gt) {
     __shared__ int total_s;
     const int e = threadIdx.x;
     int tot = 0;
@@ -391,18 +403,23 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(const int32_t* __restri
     }
 }
 
-__global__ void __launch_bounds__(128) perm_scatter_kernel(const int32_t* __restrict__ ids, int T, int E, int k,
-                                                           int n_chunks, const int32_t* __restrict__ chunk_base,
-                                                           const int32_t* __restrict__ offsets,
-                                                           const int32_t* __restrict__ offsets_pad,
-                                                           int32_t* __restrict__ sorted_token,
-                                                           int32_t* __restrict__ inv_row,
-                                                           int32_t* __restrict__ inv_int, uint32_t* status) {
-    extern __shared__ int32_t run_smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int c = blockIdx.x * 4 + warp;
-    if (c >= n_chunks) return;
-    int32_t* run = run_smem + warp * E;
+__global__ void __launch_bounds__(1024) perm_scan_kernel(const int32_t* __restrict__ chunk_cnt, int n_chunks, int T,
+                                                         int E, int k, int n_shared, int bn,
+                                                         int32_t* __restrict__ chunk_base,
+                                                         int32_t* __restrict__ offsets,
+                                                         int32_t* __restrict__ offsets_pad,
+                                                         int32_t* __restrict__ offsets_out, GroupTable* gt) {
+    scan_groups(chunk_cnt, n_chunks, T, E, k, n_shared, bn, chunk_base, offsets, offsets_pad, offsets_out, gt);
+}
+
+// One warp scatters chunk c: stable ranks within each expert from match_any
+// over 32 assignments at a time and a running count per expert (E ints of
+// shared memory in `run`).
+__device__ void scatter_chunk(const int32_t* __restrict__ ids, int T, int E, int k, int c,
+                              const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ offsets,
+                              const int32_t* __restrict__ offsets_pad, int32_t* __restrict__ sorted_token,
+                              int32_t* __restrict__ inv_row, int32_t* __restrict__ inv_int, uint32_t* status,
+                              int32_t* run, int lane) {
     for (int e = lane; e < E; e += 32) run[e] = 0;
     __syncwarp();
     const int t0 = c * CHUNK_TOK;
@@ -426,6 +443,77 @@ __global__ void __launch_bounds__(128) perm_scatter_kernel(const int32_t* __rest
         if (valid && (peers & lt_mask) == 0) run[e] += __popc(peers);
         __syncwarp();
     }
+}
+
+__global__ void __launch_bounds__(128) perm_scatter_kernel(const int32_t* __restrict__ ids, int T, int E, int k,
+                                                           int n_chunks, const int32_t* __restrict__ chunk_base,
+                                                           const int32_t* __restrict__ offsets,
+                                                           const int32_t* __restrict__ offsets_pad,
+                                                           int32_t* __restrict__ sorted_token,
+                                                           int32_t* __restrict__ inv_row,
+                                                           int32_t* __restrict__ inv_int, uint32_t* status) {
+    extern __shared__ int32_t run_smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x * 4 + warp;
+    if (c >= n_chunks) return;
+    scatter_chunk(ids, T, E, k, c, chunk_base, offsets, offsets_pad, sorted_token, inv_row, inv_int, status,
+                  run_smem + warp * E, lane);
+}
+
+// ---------------------------------------------------------------------------
+// Routing of a decode batch (T <= CHUNK_TOK, E <= 512) in one CTA: top-k and
+// gate weights, then the grouping (count, scan, scatter) of the single
+// chunk -- the same device functions as the multi-CTA kernels above, so the
+// results are identical, with three kernel boundaries fewer.
+// ---------------------------------------------------------------------------
+constexpr int SMALL_THREADS = 512;
+
+template <int PER>
+__global__ void __launch_bounds__(SMALL_THREADS) route_small_kernel(
+    const float* __restrict__ part, int ksplit, const float* __restrict__ bias, int T, int E, int k, int n_shared,
+    int bn, float* __restrict__ logits_out, int32_t* __restrict__ ids, float* __restrict__ wout,
+    int32_t* __restrict__ chunk_cnt, int32_t* __restrict__ chunk_base, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ offsets_pad, int32_t* __restrict__ offsets_out, GroupTable* gt,
+    int32_t* __restrict__ sorted_token, int32_t* __restrict__ inv_row, int32_t* __restrict__ inv_int,
+    uint32_t* status) {
+    __shared__ float sel_v[SMALL_THREADS / 32][MAX_TOPK];
+    __shared__ int sel_i[SMALL_THREADS / 32][MAX_TOPK];
+    __shared__ int32_t cnt[512];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int t = warp; t < T; t += SMALL_THREADS / 32)
+        topk_token<PER>(part, ksplit, bias, T, E, k, logits_out, ids, wout, t, lane, sel_v[warp], sel_i[warp]);
+    __syncthreads();
+    if (warp == 0) count_chunk(ids, T, E, k, 0, cnt, chunk_cnt, status, lane);
+    __syncthreads();
+    scan_groups(chunk_cnt, 1, T, E, k, n_shared, bn, chunk_base, offsets, offsets_pad, offsets_out, gt);
+    __syncthreads();
+    if (warp == 0)
+        scatter_chunk(ids, T, E, k, 0, chunk_base, offsets, offsets_pad, sorted_token, inv_row, inv_int, status, cnt,
+                      lane);
+}
+
+cudaError_t launch_route_small(const moe_layer* L, const float* part, int ksplit, bool add_bias, int T,
+                               float* logits_out, int32_t* ids, float* w, const WsLayout& lay, char* ws, int bn,
+                               int32_t* offsets_out, int32_t* sorted_out, int32_t* inv_out, cudaStream_t s) {
+    const int E = L->d.n_experts, k = L->d.top_k;
+    int32_t* inv_row = reinterpret_cast<int32_t*>(ws + lay.inv_row);
+    const int per = (E + 31) / 32;
+#define MOE_SMALL_CASE(P)                                                                                         \
+    if (per <= P) {                                                                                               \
+        route_small_kernel<P><<<1, SMALL_THREADS, 0, s>>>(                                                        \
+            part, ksplit, add_bias ? L->router_b : nullptr, T, E, k, L->d.n_shared, bn, logits_out, ids, w,       \
+            reinterpret_cast<int32_t*>(ws + lay.chunk_cnt), reinterpret_cast<int32_t*>(ws + lay.chunk_base),      \
+            reinterpret_cast<int32_t*>(ws + lay.offsets), reinterpret_cast<int32_t*>(ws + lay.offsets_pad),       \
+            offsets_out, reinterpret_cast<GroupTable*>(ws + lay.table), sorted_out, inv_row,                      \
+            reinterpret_cast<int32_t*>(ws + lay.inv_int), L->dev_status);                                         \
+    } else
+    MOE_SMALL_CASE(1) MOE_SMALL_CASE(2) MOE_SMALL_CASE(4) MOE_SMALL_CASE(8) MOE_SMALL_CASE(12) MOE_SMALL_CASE(16)
+    return cudaErrorInvalidValue;
+#undef MOE_SMALL_CASE
+    cudaError_t err = cudaGetLastError();
+    if (err == cudaSuccess && inv_out)
+        err = cudaMemcpyAsync(inv_out, inv_row, sizeof(int32_t) * (size_t)T * k, cudaMemcpyDeviceToDevice, s);
+    return err;
 }
 
 cudaError_t launch_permute(const moe_layer* L, const int32_t* ids, int T, const WsLayout& lay, char* ws, int bn,
