@@ -557,9 +557,12 @@ cudaError_t launch_permute(const moe_layer* L, const int32_t* ids, int T, const 
 // for the routed groups and shared_row0 + t for the shared group; the codes
 // go to the swizzled K-block-major layout (see act_offset) and the scales
 // to sxT[g][row], so one tile of rows is one contiguous run of both.  CTA
-// (token, blockIdx.y) quantises groups 8*blockIdx.y .. +7, one warp per
-// group, 4 channels per lane.
+// (token, blockIdx.y) quantises groups 32 blockIdx.y .. +31, warp w the
+// groups w, w + 8, w + 16, w + 24 of them (loads issued together), 4
+// channels per lane.
 // ---------------------------------------------------------------------------
+constexpr int QUANT_GPW = 4;    // 128-channel groups per warp (loads in flight per lane)
+
 __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __restrict__ x, int T, int H, int k,
                                                             int n_shared, const int32_t* __restrict__ inv_int,
                                                             const int32_t* __restrict__ offsets_pad, int E,
@@ -574,8 +577,18 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __re
     if (threadIdx.x == 0 && n_shared) dest[k] = offsets_pad[E] + t;
     __syncthreads();
     const int G = H / QB;
-    for (int g = blockIdx.y * 8 + warp; g < G; g += 8 * gridDim.y) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(x + (size_t)t * H + g * QB + lane * 4);
+    // warp w of CTA (t, y) quantises groups 32y + w + 8i, i < QUANT_GPW; their loads are issued first
+    uint2 raws[QUANT_GPW];
+#pragma unroll
+    for (int i = 0; i < QUANT_GPW; ++i) {
+        const int g = blockIdx.y * 8 * QUANT_GPW + warp + 8 * i;
+        raws[i] = g < G ? *reinterpret_cast<const uint2*>(x + (size_t)t * H + g * QB + lane * 4) : make_uint2(0u, 0u);
+    }
+#pragma unroll
+    for (int i = 0; i < QUANT_GPW; ++i) {
+        const int g = blockIdx.y * 8 * QUANT_GPW + warp + 8 * i;
+        if (g >= G) break;
+        const uint2 raw = raws[i];
         const float v0 = __uint_as_float(raw.x << 16), v1 = __uint_as_float(raw.x & 0xFFFF0000u);
         const float v2 = __uint_as_float(raw.y << 16), v3 = __uint_as_float(raw.y & 0xFFFF0000u);
         float a = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
@@ -597,8 +610,8 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __re
 cudaError_t launch_quant_scatter(const moe_layer* L, const uint16_t* x, int T, const WsLayout& lay, char* ws,
                                  uint8_t* xq_out, float* sx_out, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    // one warp per 128-channel group: grid.y covers the groups 8 at a time
-    const dim3 grid(T, (L->d.hidden / QB + 7) / 8);
+    // one warp per 128-channel group, QUANT_GPW groups per warp: grid.y covers the groups 8 * QUANT_GPW at a time
+    const dim3 grid(T, (L->d.hidden / QB + 8 * QUANT_GPW - 1) / (8 * QUANT_GPW));
     quant_scatter_kernel<<<grid, 256, 0, s>>>(x, T, L->d.hidden, L->d.top_k, L->d.n_shared,
                                            reinterpret_cast<const int32_t*>(ws + lay.inv_int),
                                            reinterpret_cast<const int32_t*>(ws + lay.offsets_pad), L->d.n_experts,
