@@ -1,8 +1,10 @@
 // Grouped FP8 expert GEMMs on sm_103a (weight-streaming path).
 //
 // One persistent CTA per SM walks the units (group, n tile of <= 64 rows,
-// m tile of 128 output features).  A producer warp streams, for every
-// 128-wide K block, the 128x128 weight tile image(s) with one bulk copy and
+// weight block): a gate/up block is the gate and up tiles of 128 inner
+// features, a down block two consecutive 128-row tiles of the output.  A
+// producer warp streams, for every 128-wide K block, the block's two
+// 128x128 weight tile images with bulk copies and
 // the unit's activation rows (128 B each) with per-row bulk copies into a
 // ring of shared-memory stages guarded by mbarriers; eight consumer warps
 // run FP8 E4M3 tensor-core MMAs (m16n8k32, fp32 accumulate) on each stage.
@@ -20,8 +22,9 @@
 // h = SiLU(g) * u (the activation and elementwise product that sit between
 // gate/up and down in the article's "CPU fine-grained parallelism"
 // section), quantises each token's 128 values of h to E4M3 with
-// s = amax/448, and writes the codes and the scale.  Down kernel: writes the
-// unweighted fp32 expert output rows.
+// s = amax/448, and writes the codes and the scale.  Down kernel: the two
+// output tiles take the places of gate and up (same fragments, second
+// accumulator) and it writes the unweighted fp32 expert output rows of both.
 //
 // K permutation inside a 128-block: lane (g, q) of a warp owns the 32
 // consecutive channels [32q, 32q+32) of the block; MMA m (0..3) takes
@@ -48,10 +51,10 @@ constexpr int TAIL = 1024;
 
 template <bool GU>
 struct Cfg {
-    static constexpr int W_BYTES = GU ? 2 * TILE_BYTES : TILE_BYTES;
+    static constexpr int W_BYTES = 2 * TILE_BYTES;      // gate + up tile, or two consecutive down tiles
     static constexpr int X_BYTES = BN * XSTRIDE;
     static constexpr int STAGE = W_BYTES + X_BYTES + TAIL;
-    static constexpr int STAGES = GU ? 5 : 7;           // as deep as shared memory allows (HBM latency)
+    static constexpr int STAGES = GU ? 5 : 4;           // as deep as shared memory allows (HBM latency)
     static constexpr int EPI = GU ? (BN * 144 + CW * BN * 4) : (BN * 132 * 4);
     // + the group table copy for up to 385 groups (larger tables are read in place)
     static constexpr int SMEM = STAGES * STAGE + EPI + gt_smem_bytes(GT_CAP_DEC) + 2 * STAGES * 8 + 128;
@@ -99,8 +102,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_gemm_kernel(ExpertArgs a) 
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int MT = a.M / QB, KT = a.K / QB;
+    // weight blocks per n tile: gate/up one 128-row tile pair (gate, up) each; down two consecutive
+    // 128-row output tiles each (the last block of an odd tile count has one)
+    const int NB = GU ? MT : (MT + 1) / 2;
     const GroupTable* gt = a.gt;
-    const int n_units = gt->n_pairs * MT;
+    const int n_units = gt->n_pairs * NB;
     const SGroups sg = load_groups(gt, gt_s, threadIdx.x, NTHREADS, GT_CAP_DEC);
 
     if (threadIdx.x == 0) {
@@ -121,20 +127,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_gemm_kernel(ExpertArgs a) 
         uint32_t armed = 0, armed_par = 0;       // per stage: armed at least once / parity of last arm
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-            const Unit un = decode_unit(sg, u, MT);
-            const uint8_t* wbase = a.w + ((size_t)(un.expert * MT + un.mb) * KT) * C::W_BYTES;
+            const Unit un = decode_unit(sg, u, NB);
+            const int t0 = GU ? un.mb : 2 * un.mb;
+            const bool two = GU || t0 + 1 < MT;
+            const uint8_t* wbase = a.w + ((size_t)(un.expert * MT + t0) * KT) * (GU ? C::W_BYTES : TILE_BYTES);
             for (int kb = 0; kb < KT; ++kb) {
                 if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, a.wait_limit, a.status, abort)) { ok = false; break; }
                 uint8_t* st = stages + stage * C::STAGE;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&full[stage], C::W_BYTES + un.valid * QB + S_BYTES + R_BYTES);
-                    bulk_g2s(st, wbase + (size_t)kb * C::W_BYTES, C::W_BYTES, &full[stage]);
+                    mbar_arrive_expect_tx(&full[stage],
+                                          (two ? 2 : 1) * TILE_BYTES + un.valid * QB + S_BYTES + R_BYTES);
+                    if (GU) {
+                        bulk_g2s(st, wbase + (size_t)kb * C::W_BYTES, C::W_BYTES, &full[stage]);
+                    } else {
+                        bulk_g2s(st, wbase + (size_t)kb * TILE_BYTES, TILE_BYTES, &full[stage]);
+                        if (two)
+                            bulk_g2s(st + TILE_BYTES, wbase + ((size_t)KT + kb) * TILE_BYTES, TILE_BYTES, &full[stage]);
+                    }
                     bulk_g2s(st + C::W_BYTES, a.act + act_offset(kb, un.row_begin, a.ld), un.valid * QB,
                              &full[stage]);
                     uint8_t* tail = st + C::W_BYTES + C::X_BYTES;
                     bulk_g2s(tail, a.actsT + (size_t)kb * a.ld + un.row_begin, S_BYTES, &full[stage]);
-                    const size_t rec = GU ? ((size_t)un.expert * MT + un.mb) * KT + kb
-                                          : ((size_t)un.expert * ((MT + 1) / 2) + (un.mb >> 1)) * KT + kb;
+                    const size_t rec = ((size_t)un.expert * NB + un.mb) * KT + kb;
                     bulk_g2s(tail + S_BYTES, a.wrec + rec * 4, R_BYTES, &full[stage]);
                 }
                 __syncwarp();
@@ -158,8 +172,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_gemm_kernel(ExpertArgs a) 
     bool dead = false;    // a wait gave up: skip the math, keep the barriers
 
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const Unit un = decode_unit(sg, u, MT);
+        const Unit un = decode_unit(sg, u, NB);
         const int nt_active = (un.valid + 7) >> 3;
+        const int t0 = GU ? un.mb : 2 * un.mb;         // down: output tiles t0 (accg) and t0 + 1 (accu)
+        const bool dual = GU || t0 + 1 < MT;
         float accg[BN / 8][4], accu[BN / 8][4];
 #pragma unroll
         for (int nt = 0; nt < BN / 8; ++nt)
@@ -174,10 +190,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_gemm_kernel(ExpertArgs a) 
             }
             const uint8_t* st = stages + stage * C::STAGE;
             // scales from the stage tail: s_x of this lane's columns, the weight-scale record
-            // (gate/up: {gate, up}; down: {tile 2b, tile 2b+1} of the pair holding this m tile)
+            // (gate/up: {gate, up}; down: {tile 2b, tile 2b+1})
             const float* tail = reinterpret_cast<const float*>(st + C::W_BYTES + C::X_BYTES);
             const float2 rec = *reinterpret_cast<const float2*>(tail + BN);
-            const float swg = GU ? rec.x : ((un.mb & 1) ? rec.y : rec.x);
+            const float swg = rec.x;
             const float swu = rec.y;
             float sa[BN / 8][2];
 #pragma unroll
@@ -192,7 +208,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_gemm_kernel(ExpertArgs a) 
             const uint32_t Ag[8] = {ag0.x, ag0.y, ag0.z, ag0.w, ag1.x, ag1.y, ag1.z, ag1.w};
             const uint32_t Ah[8] = {ag8.x, ag8.y, ag8.z, ag8.w, ag9.x, ag9.y, ag9.z, ag9.w};
             uint32_t Bg[8] = {0, 0, 0, 0, 0, 0, 0, 0}, Bh[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            if (GU) {
+            if (dual) {
                 const uint8_t* U = st + TILE_BYTES;
                 const uint4 au0 = lds128(U + r0 * 128 + c0), au1 = lds128(U + r0 * 128 + c1);
                 const uint4 au8 = lds128(U + (r0 + 8) * 128 + c0), au9 = lds128(U + (r0 + 8) * 128 + c1);
@@ -217,7 +233,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_gemm_kernel(ExpertArgs a) 
                     accg[nt][1] = __fmaf_rn(pg[1], s1, accg[nt][1]);
                     accg[nt][2] = __fmaf_rn(pg[2], s0, accg[nt][2]);
                     accg[nt][3] = __fmaf_rn(pg[3], s1, accg[nt][3]);
-                    if (GU) {
+                    if (dual) {
                         float pu[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                         for (int m = 0; m < 4; ++m)
@@ -288,25 +304,32 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_gemm_kernel(ExpertArgs a) 
             }
             named_bar_sync(1, CW * 32);
         } else {
-            // ---------------------------------------------- fp32 expert output rows
+            // ---------------------------------------------- fp32 expert output rows: tile t0 from accg,
+            // tile t0 + 1 from accu, each staged through shared memory and stored row by row
             float* ost = reinterpret_cast<float*>(epi);           // [BN][132]
 #pragma unroll
-            for (int nt = 0; nt < BN / 8; ++nt) {
-                if (nt < nt_active) {
-                    const int col = nt * 8 + 2 * q;
-                    ost[col * 132 + r0] = accg[nt][0];
-                    ost[(col + 1) * 132 + r0] = accg[nt][1];
-                    ost[col * 132 + r0 + 8] = accg[nt][2];
-                    ost[(col + 1) * 132 + r0 + 8] = accg[nt][3];
+            for (int part = 0; part < 2; ++part) {
+                if (part == 1 && !dual) break;
+                const float(&acc)[BN / 8][4] = part ? accu : accg;
+#pragma unroll
+                for (int nt = 0; nt < BN / 8; ++nt) {
+                    if (nt < nt_active) {
+                        const int col = nt * 8 + 2 * q;
+                        ost[col * 132 + r0] = acc[nt][0];
+                        ost[(col + 1) * 132 + r0] = acc[nt][1];
+                        ost[col * 132 + r0 + 8] = acc[nt][2];
+                        ost[(col + 1) * 132 + r0 + 8] = acc[nt][3];
+                    }
                 }
+                named_bar_sync(1, CW * 32);
+                const int tid = threadIdx.x;
+                for (int rr = tid >> 5; rr < un.valid; rr += (CW * 32) >> 5) {
+                    const float4 v = *reinterpret_cast<const float4*>(ost + rr * 132 + (tid & 31) * 4);
+                    *reinterpret_cast<float4*>(a.out + (size_t)(un.row_begin + rr) * a.M + (t0 + part) * QB +
+                                               (tid & 31) * 4) = v;
+                }
+                named_bar_sync(1, CW * 32);
             }
-            named_bar_sync(1, CW * 32);
-            const int tid = threadIdx.x;
-            for (int rr = tid >> 5; rr < un.valid; rr += (CW * 32) >> 5) {
-                const float4 v = *reinterpret_cast<const float4*>(ost + rr * 132 + (tid & 31) * 4);
-                *reinterpret_cast<float4*>(a.out + (size_t)(un.row_begin + rr) * a.M + un.mb * QB + (tid & 31) * 4) = v;
-            }
-            named_bar_sync(1, CW * 32);
         }
     }
 }
