@@ -34,7 +34,8 @@
  *    (NULL = the legacy default stream).
  *  - Asynchrony: calls validate their arguments on the host, enqueue work on
  *    the given stream and return; nothing waits for the GPU except
- *    moe_create, moe_destroy, moe_get_device_status and moe_forward_host.
+ *    moe_create(_ex), moe_destroy, moe_get_device_status, moe_profile_read
+ *    and moe_forward_host.
  *  - Ownership: moe_create copies (and repacks) every weight into memory
  *    the layer owns; the caller may free its weight buffers once it
  *    returns.  Activations, outputs and the workspace are caller-owned;

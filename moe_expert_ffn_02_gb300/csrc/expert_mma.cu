@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_gemm_kernel(ExpertArgs a) 
     // 128-row output tiles each (the last block of an odd tile count has one)
     const int NB = GU ? MT : (MT + 1) / 2;
     const GroupTable* gt = a.gt;
+    pdl_wait();                                   // the group table and activations come from earlier kernels
     const int n_units = gt->n_pairs * NB;
     const SGroups sg = load_groups(gt, gt_s, threadIdx.x, NTHREADS, GT_CAP_DEC);
 
@@ -335,7 +336,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_gemm_kernel(ExpertArgs a) 
 }
 
 template <bool GU>
-static cudaError_t launch_expert(const moe_layer* L, const WsLayout& lay, char* ws, int max_units, cudaStream_t s) {
+static cudaError_t launch_expert(const moe_layer* L, const WsLayout& lay, char* ws, cudaStream_t s) {
     using C = Cfg<GU>;
     static bool attr_set[2] = {false, false};
     if (!attr_set[GU]) {
@@ -364,24 +365,20 @@ static cudaError_t launch_expert(const moe_layer* L, const WsLayout& lay, char* 
         a.actsT = reinterpret_cast<const float*>(ws + lay.shT);
         a.K = I; a.M = H;
     }
-    int grid = L->num_sms;
-    if (max_units > 0 && max_units < grid) grid = max_units;
-    expert_gemm_kernel<GU><<<grid, NTHREADS, C::SMEM + 1024, s>>>(a);
-    return cudaGetLastError();
+    const int grid = L->num_sms;
+    return launch_pdl(expert_gemm_kernel<GU>, dim3(grid), dim3(NTHREADS), C::SMEM + 1024, s, a);
 }
 
-cudaError_t launch_expert_gate_up(const moe_layer* L, int T, const WsLayout& lay, char* ws, int bn, int max_units,
-                                  cudaStream_t s) {
+cudaError_t launch_expert_gate_up(const moe_layer* L, int T, const WsLayout& lay, char* ws, int bn, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    if (bn != BN) return cudaErrorInvalidValue;
-    return launch_expert<true>(L, lay, ws, max_units, s);
+    if (bn != BN) return cudaErrorInvalidValue;       // the group table must be built for BN-row tiles
+    return launch_expert<true>(L, lay, ws, s);
 }
 
-cudaError_t launch_expert_down(const moe_layer* L, int T, const WsLayout& lay, char* ws, int bn, int max_units,
-                               cudaStream_t s) {
+cudaError_t launch_expert_down(const moe_layer* L, int T, const WsLayout& lay, char* ws, int bn, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     if (bn != BN) return cudaErrorInvalidValue;
-    return launch_expert<false>(L, lay, ws, max_units, s);
+    return launch_expert<false>(L, lay, ws, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -398,6 +395,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     __shared__ int rows[MAX_TOPK];
     __shared__ float wt[MAX_TOPK];
     const int t = blockIdx.x;
+    pdl_trigger();
+    pdl_wait();
     if (threadIdx.x < k) {
         rows[threadIdx.x] = inv_int[(size_t)t * k + threadIdx.x];
         wt[threadIdx.x] = w[(size_t)t * k + threadIdx.x];
@@ -427,12 +426,11 @@ cudaError_t launch_combine(const moe_layer* L, int T, const WsLayout& lay, char*
     if (T == 0) return cudaSuccess;
     // CTA (token, blockIdx.y) owns channels [1024 blockIdx.y, +1024): one float4 per thread
     const dim3 grid(T, (L->d.hidden + 1023) / 1024);
-    combine_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const float*>(ws + lay.o),
+    return launch_pdl(combine_kernel, grid, dim3(256), 0, s, reinterpret_cast<const float*>(ws + lay.o),
                                      reinterpret_cast<const int32_t*>(ws + lay.inv_int),
                                      reinterpret_cast<const float*>(ws + lay.w),
                                      reinterpret_cast<const int32_t*>(ws + lay.offsets_pad), T, L->d.hidden, L->d.top_k,
                                      L->d.n_experts, L->d.n_shared, y);
-    return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
@@ -463,6 +461,8 @@ __global__ void __launch_bounds__(256) combine_split_kernel(const float* __restr
     __shared__ int rows[MAX_TOPK], part_of[MAX_TOPK];
     __shared__ float wt[MAX_TOPK];
     const int t = blockIdx.x;
+    pdl_trigger();
+    pdl_wait();
     if (threadIdx.x < k) {
         const int j = threadIdx.x;
         rows[j] = inv_int[(size_t)t * k + j];
@@ -521,12 +521,11 @@ cudaError_t launch_combine_split(const moe_layer* L, int T, const WsLayout& lay,
                                  const uint8_t* defer, uint16_t* y, uint16_t* y_next, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     const dim3 grid(T, (L->d.hidden + 1023) / 1024);
-    combine_split_kernel<<<grid, 256, 0, s>>>(
+    return launch_pdl(combine_split_kernel, grid, dim3(256), 0, s, 
         reinterpret_cast<const float*>(ws + lay.o), reinterpret_cast<const int32_t*>(ws + lay.inv_int),
         reinterpret_cast<const int32_t*>(ws + lay.ids), reinterpret_cast<const float*>(ws + lay.w),
         reinterpret_cast<const int32_t*>(ws + lay.offsets_pad), defer, T, L->d.hidden, L->d.top_k, L->d.n_experts,
         L->d.n_shared, n_ranks, y, y_next);
-    return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------

@@ -130,6 +130,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
     const int MT128 = a.M / QB;                              // 128-row weight tiles per expert
     const int NB = GU ? MT128 : (MT128 + 1) / 2;             // weight blocks per unit row
     const GroupTable* gt = a.gt;
+    pdl_wait();                                   // the group table and activations come from earlier kernels
     const int n_units = gt->n_pairs * NB;
     const SGroups sg = load_groups(gt, gt_s, threadIdx.x, NTHREADS, GT_SMEM_CAP);
 
@@ -391,8 +392,7 @@ static cudaError_t launch(const moe_layer* L, const WsLayout& lay, char* ws, cud
         a.actsT = reinterpret_cast<const float*>(ws + lay.shT);
         a.K = I; a.M = H;
     }
-    expert_tc_kernel<GU><<<L->num_sms, NTHREADS, SMEM + 1024, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(expert_tc_kernel<GU>, dim3(L->num_sms), dim3(NTHREADS), SMEM + 1024, s, a);
 }
 
 // Weight-scale records, built once at load time from the repacked scales:

@@ -252,6 +252,17 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
+// Programmatic dependent launch.  Kernels of the forward path are launched
+// with launch_pdl; each calls pdl_wait() before it reads anything the
+// preceding kernel wrote (the wait returns once that grid has completed and
+// its memory is visible), so the launch, and whatever the kernel does before
+// the wait, overlaps the preceding kernel.  Small kernels call pdl_trigger()
+// on entry so their successor is launched at once; the persistent GEMMs
+// trigger by exiting.  Both are no-ops for a kernel launched without the
+// attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -299,6 +310,24 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(
 
 // Launchers (defined in the .cu files, called from api.cu).
 namespace moe {
+
+// Launch with programmatic stream serialisation (see pdl_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 cudaError_t launch_repack(const moe_layer* L, const moe_weights* w, cudaStream_t s);
 int router_gemv_splits(int H);
 int router_tc_splits(int T, int H, int E, int num_sms);
@@ -316,10 +345,8 @@ cudaError_t launch_permute(const moe_layer* L, const int32_t* ids, int T, const 
                            int32_t* offsets_out, int32_t* sorted_out, int32_t* inv_out, cudaStream_t s);
 cudaError_t launch_quant_scatter(const moe_layer* L, const uint16_t* x, int T, const WsLayout& lay, char* ws,
                                  uint8_t* xq_out, float* sx_out, cudaStream_t s);
-cudaError_t launch_expert_gate_up(const moe_layer* L, int T, const WsLayout& lay, char* ws, int bn, int max_units,
-                                  cudaStream_t s);
-cudaError_t launch_expert_down(const moe_layer* L, int T, const WsLayout& lay, char* ws, int bn, int max_units,
-                               cudaStream_t s);
+cudaError_t launch_expert_gate_up(const moe_layer* L, int T, const WsLayout& lay, char* ws, int bn, cudaStream_t s);
+cudaError_t launch_expert_down(const moe_layer* L, int T, const WsLayout& lay, char* ws, int bn, cudaStream_t s);
 cudaError_t launch_h_gather(const moe_layer* L, int T, const WsLayout& lay, char* ws, uint8_t* hq_out, float* sh_out,
                             cudaStream_t s);
 int tc_tile_n();

@@ -31,6 +31,8 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) router_gemv_kernel(const uint
                                                                       int E, int slice, int tc,
                                                                       float* __restrict__ part) {
     extern __shared__ __align__(16) uint16_t xs[];              // [tc][slice]
+    pdl_trigger();
+    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x * GEMV_WARPS + warp;
     const int z = blockIdx.y;
@@ -109,8 +111,8 @@ cudaError_t launch_router_logits(const moe_layer* L, const uint16_t* x, int T, f
             attr = true;
         }
         dim3 grid((E + GEMV_WARPS - 1) / GEMV_WARPS, ksplit);
-        router_gemv_kernel<<<grid, GEMV_WARPS * 32, smem, s>>>(x, L->router_w, T, H, E, slice, tc, part);
-        return cudaGetLastError();
+        return launch_pdl(router_gemv_kernel, grid, dim3(GEMV_WARPS * 32), smem, s, x, L->router_w, T, H, E, slice, tc,
+                          part);
     }
     return launch_router_tc(L, x, T, part, ksplit, s);      // prefill batch: tensor-core GEMM (router_tc.cu)
 }
@@ -239,6 +241,8 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
     __shared__ int sel_i[8][MAX_TOPK];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
+    pdl_trigger();
+    pdl_wait();
     if (t >= T) return;
     topk_token<PER>(part, ksplit, bias, T, E, k, logits_out, ids, wout, t, lane, sel_v[warp], sel_i[warp]);
 }
@@ -252,8 +256,7 @@ cudaError_t launch_topk(const moe_layer* L, const float* part, int ksplit, bool 
     dim3 grid((T + 7) / 8);
 #define MOE_TOPK_CASE(P)                                                                              \
     if (per <= P) {                                                                                   \
-        topk_kernel<P><<<grid, 256, 0, s>>>(part, ksplit, bias, T, E, k, logits_out, ids, w);         \
-        return cudaGetLastError();                                                                    \
+        return launch_pdl(topk_kernel<P>, grid, dim3(256), 0, s, part, ksplit, bias, T, E, k, logits_out, ids, w); \
     }
     MOE_TOPK_CASE(1) MOE_TOPK_CASE(2) MOE_TOPK_CASE(4) MOE_TOPK_CASE(8) MOE_TOPK_CASE(12)
     MOE_TOPK_CASE(16) MOE_TOPK_CASE(24) MOE_TOPK_CASE(32)
@@ -306,6 +309,8 @@ __global__ void __launch_bounds__(128) perm_count_kernel(const int32_t* __restri
     extern __shared__ int32_t cnt_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x * 4 + warp;
+    pdl_trigger();
+    pdl_wait();
     if (c >= n_chunks) return;
     count_chunk(ids, T, E, k, c, cnt_smem + warp * E, chunk_cnt, status, lane);
 }
@@ -409,6 +414,8 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(const int32_t* __restri
                                                          int32_t* __restrict__ offsets,
                                                          int32_t* __restrict__ offsets_pad,
                                                          int32_t* __restrict__ offsets_out, GroupTable* gt) {
+    pdl_trigger();
+    pdl_wait();
     scan_groups(chunk_cnt, n_chunks, T, E, k, n_shared, bn, chunk_base, offsets, offsets_pad, offsets_out, gt);
 }
 
@@ -455,6 +462,8 @@ __global__ void __launch_bounds__(128) perm_scatter_kernel(const int32_t* __rest
     extern __shared__ int32_t run_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x * 4 + warp;
+    pdl_trigger();
+    pdl_wait();
     if (c >= n_chunks) return;
     scatter_chunk(ids, T, E, k, c, chunk_base, offsets, offsets_pad, sorted_token, inv_row, inv_int, status,
                   run_smem + warp * E, lane);
@@ -480,6 +489,8 @@ __global__ void __launch_bounds__(SMALL_THREADS) route_small_kernel(
     __shared__ int sel_i[SMALL_THREADS / 32][MAX_TOPK];
     __shared__ int32_t cnt[512];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_trigger();
+    pdl_wait();
     for (int t = warp; t < T; t += SMALL_THREADS / 32)
         topk_token<PER>(part, ksplit, bias, T, E, k, logits_out, ids, wout, t, lane, sel_v[warp], sel_i[warp]);
     __syncthreads();
@@ -500,17 +511,17 @@ cudaError_t launch_route_small(const moe_layer* L, const float* part, int ksplit
     const int per = (E + 31) / 32;
 #define MOE_SMALL_CASE(P)                                                                                         \
     if (per <= P) {                                                                                               \
-        route_small_kernel<P><<<1, SMALL_THREADS, 0, s>>>(                                                        \
+        err = launch_pdl(route_small_kernel<P>, dim3(1), dim3(SMALL_THREADS), 0, s,                               \
             part, ksplit, add_bias ? L->router_b : nullptr, T, E, k, L->d.n_shared, bn, logits_out, ids, w,       \
             reinterpret_cast<int32_t*>(ws + lay.chunk_cnt), reinterpret_cast<int32_t*>(ws + lay.chunk_base),      \
             reinterpret_cast<int32_t*>(ws + lay.offsets), reinterpret_cast<int32_t*>(ws + lay.offsets_pad),       \
             offsets_out, reinterpret_cast<GroupTable*>(ws + lay.table), sorted_out, inv_row,                      \
             reinterpret_cast<int32_t*>(ws + lay.inv_int), L->dev_status);                                         \
     } else
+    cudaError_t err = cudaSuccess;
     MOE_SMALL_CASE(1) MOE_SMALL_CASE(2) MOE_SMALL_CASE(4) MOE_SMALL_CASE(8) MOE_SMALL_CASE(12) MOE_SMALL_CASE(16)
     return cudaErrorInvalidValue;
 #undef MOE_SMALL_CASE
-    cudaError_t err = cudaGetLastError();
     if (err == cudaSuccess && inv_out)
         err = cudaMemcpyAsync(inv_out, inv_row, sizeof(int32_t) * (size_t)T * k, cudaMemcpyDeviceToDevice, s);
     return err;
@@ -530,18 +541,16 @@ cudaError_t launch_permute(const moe_layer* L, const int32_t* ids, int T, const 
     const int nc = lay.n_chunks;
     const size_t smem = 4 * E * sizeof(int32_t);
     if (nc > 0) {
-        perm_count_kernel<<<(nc + 3) / 4, 128, smem, s>>>(ids, T, E, k, nc, chunk_cnt, L->dev_status);
-        cudaError_t err = cudaGetLastError();
+        cudaError_t err = launch_pdl(perm_count_kernel, dim3((nc + 3) / 4), dim3(128), smem, s, ids, T, E, k, nc,
+                                     chunk_cnt, L->dev_status);
         if (err != cudaSuccess) return err;
     }
-    perm_scan_kernel<<<1, 1024, 0, s>>>(chunk_cnt, nc, T, E, k, L->d.n_shared, bn, chunk_base, offsets, offsets_pad,
-                                        offsets_out, gt);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = launch_pdl(perm_scan_kernel, dim3(1), dim3(1024), 0, s, chunk_cnt, nc, T, E, k, L->d.n_shared,
+                                 bn, chunk_base, offsets, offsets_pad, offsets_out, gt);
     if (err != cudaSuccess) return err;
     if (nc > 0) {
-        perm_scatter_kernel<<<(nc + 3) / 4, 128, smem, s>>>(ids, T, E, k, nc, chunk_base, offsets, offsets_pad,
-                                                            sorted_token, inv_row, inv_int, L->dev_status);
-        err = cudaGetLastError();
+        err = launch_pdl(perm_scatter_kernel, dim3((nc + 3) / 4), dim3(128), smem, s, ids, T, E, k, nc, chunk_base,
+                         offsets, offsets_pad, sorted_token, inv_row, inv_int, L->dev_status);
         if (err != cudaSuccess) return err;
         if (inv_out)
             err = cudaMemcpyAsync(inv_out, inv_row, sizeof(int32_t) * (size_t)T * k, cudaMemcpyDeviceToDevice, s);
@@ -572,6 +581,8 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __re
     __shared__ int dest[MAX_TOPK + 1];
     const int t = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_trigger();
+    pdl_wait();
     const int nd = k + (n_shared ? 1 : 0);
     if (threadIdx.x < k) dest[threadIdx.x] = inv_int[(size_t)t * k + threadIdx.x];
     if (threadIdx.x == 0 && n_shared) dest[k] = offsets_pad[E] + t;
@@ -612,12 +623,11 @@ cudaError_t launch_quant_scatter(const moe_layer* L, const uint16_t* x, int T, c
     if (T == 0) return cudaSuccess;
     // one warp per 128-channel group, QUANT_GPW groups per warp: grid.y covers the groups 8 * QUANT_GPW at a time
     const dim3 grid(T, (L->d.hidden / QB + 8 * QUANT_GPW - 1) / (8 * QUANT_GPW));
-    quant_scatter_kernel<<<grid, 256, 0, s>>>(x, T, L->d.hidden, L->d.top_k, L->d.n_shared,
+    return launch_pdl(quant_scatter_kernel, grid, dim3(256), 0, s, x, T, L->d.hidden, L->d.top_k, L->d.n_shared,
                                            reinterpret_cast<const int32_t*>(ws + lay.inv_int),
                                            reinterpret_cast<const int32_t*>(ws + lay.offsets_pad), L->d.n_experts,
                                            reinterpret_cast<uint8_t*>(ws + lay.xp),
                                            reinterpret_cast<float*>(ws + lay.sxT), lay.rows_pad, xq_out, sx_out);
-    return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -77,6 +77,7 @@ __global__ void __launch_bounds__(NTHREADS) router_tc_kernel(const __grid_consta
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e0 = blockIdx.x * BN, t0 = blockIdx.y * BM, z = blockIdx.z;
+    pdl_wait();                                   // x may come from the preceding kernel
     const int kx0 = z * ksteps * BK;
 
     if (threadIdx.x == 0) {
@@ -279,8 +280,8 @@ cudaError_t launch_router_tc(const moe_layer* L, const uint16_t* x, int T, float
     }
     const int ksteps = H / rt::BK / ksplit;
     dim3 grid((E + rt::BN - 1) / rt::BN, (T + rt::BM - 1) / rt::BM, ksplit);
-    rt::router_tc_kernel<<<grid, rt::NTHREADS, rt::SMEM, s>>>(tx, tw, T, E, ksteps, part, L->dev_status, L->wait_limit);
-    return cudaGetLastError();
+    return launch_pdl(rt::router_tc_kernel, grid, dim3(rt::NTHREADS), rt::SMEM, s, tx, tw, T, E, ksteps, part,
+                      L->dev_status, L->wait_limit);
 }
 
 }  // namespace moe
