@@ -287,14 +287,21 @@ moe_status moe_set_wait_limit(moe_layer* layer, uint32_t microseconds);
 moe_status moe_debug_timeout_probe(moe_layer* layer, void* stream);
 
 /* Measurement hook.  With profiling enabled, every forward call records a
- * CUDA event on its stream before its first kernel and after each stage:
+ * CUDA event on its stream at the boundaries of the timed stages:
  *   stage 0 routing (logits, top-k, grouping)   stage 1 x quantisation
  *   stage 2 gate/up GEMM + SiLU*up              stage 3 down GEMM
  *   stage 4 combine
+ * `enable`: 0 disables; 1 times every stage; MOE_PROFILE_SELECT | mask
+ * times only the stages whose bits (1 << s) are set in mask.  An event
+ * between two kernels removes their programmatic-dependent-launch overlap
+ * (a few microseconds each at decode sizes), so timing only the stage of
+ * interest disturbs the layer least.  Other values: MOE_ERR_INVALID_ARG.
  * moe_profile_read synchronises the stream of the most recent call and
- * writes the elapsed milliseconds of its MOE_PROFILE_STAGES stages.
- * Enabling creates the events (no device memory); disabled by default. */
+ * writes the elapsed milliseconds of its first n_stages stages, -1 for a
+ * stage that is not timed.  Enabling creates the events (no device
+ * memory); disabled by default. */
 #define MOE_PROFILE_STAGES 5
+#define MOE_PROFILE_SELECT 0x40000000
 moe_status moe_profile_enable(moe_layer* layer, int32_t enable);
 moe_status moe_profile_read(moe_layer* layer, float* stage_ms, int32_t n_stages);
 

@@ -260,12 +260,26 @@ def moe_debug_timeout_probe(layer: int, stream: int = 0) -> None:
 PROFILE_STAGES = ("route", "quant_x", "gate_up", "down", "combine")
 
 
-def moe_profile_enable(layer: int, enable: bool = True) -> None:
-    _check(load().moe_profile_enable(layer, 1 if enable else 0))
+PROFILE_SELECT = 0x40000000
+
+
+def moe_profile_enable(layer: int, enable: bool = True, stages=None) -> None:
+    """Record stage events in forward calls: every stage, or only the named
+    ones (e.g. stages=("gate_up",)); enable=False turns profiling off."""
+    if not enable:
+        code = 0
+    elif stages is None:
+        code = 1
+    else:
+        code = PROFILE_SELECT
+        for name in stages:
+            code |= 1 << PROFILE_STAGES.index(name)
+    _check(load().moe_profile_enable(layer, code))
 
 
 def moe_profile_read(layer: int):
-    """Elapsed ms of each stage of the most recent forward call (dict)."""
+    """Elapsed ms of each stage of the most recent forward call (dict); -1
+    for a stage that is not timed."""
     buf = (ctypes.c_float * len(PROFILE_STAGES))()
     _check(load().moe_profile_read(layer, buf, len(PROFILE_STAGES)))
     return dict(zip(PROFILE_STAGES, [float(v) for v in buf]))

@@ -172,8 +172,11 @@ moe_status run_forward(moe_layer* L, int mode, const uint16_t* x, int T, uint16_
         return MOE_OK;
     }
     char* ws = static_cast<char*>(ws_v);
+    // event i opens stage i and closes stage i - 1; only the timed stages' events are recorded,
+    // so an event-free stage boundary keeps its programmatic-dependent-launch overlap
     auto mark = [&](int i) -> cudaError_t {
-        if (!L->profile) return cudaSuccess;
+        const uint32_t m = L->profile;
+        if (!(((m >> i) & 1u) || (i > 0 && ((m >> (i - 1)) & 1u)))) return cudaSuccess;
         L->ev_stream = s;
         // inside a stream capture the events become record nodes of the graph (recorded at each launch)
         cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
@@ -541,15 +544,24 @@ MOE_EXPORT moe_status moe_set_wait_limit(moe_layer* L, uint32_t limit) {
 MOE_EXPORT moe_status moe_profile_enable(moe_layer* L, int32_t enable) {
     moe_status st = check_layer(L);
     if (st != MOE_OK) return st;
-    if (enable && !L->profile) {
+    const uint32_t all = (1u << MOE_PROFILE_STAGES) - 1u;
+    uint32_t mask = 0;
+    if (enable == 1) {
+        mask = all;
+    } else if (enable != 0) {
+        if (!(enable & MOE_PROFILE_SELECT) || (enable & ~(MOE_PROFILE_SELECT | (int32_t)all)) != 0 ||
+            (enable & (int32_t)all) == 0)
+            return fail(MOE_ERR_INVALID_ARG, "profile selector %#x names no stage or an unknown one", (unsigned)enable);
+        mask = (uint32_t)enable & all;
+    }
+    if (mask && !L->profile) {
         for (int i = 0; i <= MOE_PROFILE_STAGES; ++i) MOE_CUDA(cudaEventCreate(&L->ev[i]), "event create");
-        L->profile = true;
         L->ev_stream = nullptr;
-    } else if (!enable && L->profile) {
+    } else if (!mask && L->profile) {
         MOE_CUDA(cudaDeviceSynchronize(), "synchronise");
         for (int i = 0; i <= MOE_PROFILE_STAGES; ++i) cudaEventDestroy(L->ev[i]);
-        L->profile = false;
     }
+    L->profile = mask;
     return MOE_OK;
 }
 
@@ -558,8 +570,16 @@ MOE_EXPORT moe_status moe_profile_read(moe_layer* L, float* stage_ms, int32_t n)
     if (st != MOE_OK) return st;
     if (!L->profile) return fail(MOE_ERR_INVALID_ARG, "profiling is not enabled");
     if (!stage_ms || n < 1 || n > MOE_PROFILE_STAGES) return fail(MOE_ERR_INVALID_ARG, "bad stage buffer");
-    MOE_CUDA(cudaEventSynchronize(L->ev[MOE_PROFILE_STAGES]), "event synchronise");
-    for (int i = 0; i < n; ++i) MOE_CUDA(cudaEventElapsedTime(&stage_ms[i], L->ev[i], L->ev[i + 1]), "elapsed");
+    int last = 0;                                       // the last recorded event closes the last timed stage
+    for (int i = 0; i < MOE_PROFILE_STAGES; ++i)
+        if ((L->profile >> i) & 1u) last = i + 1;
+    MOE_CUDA(cudaEventSynchronize(L->ev[last]), "event synchronise");
+    for (int i = 0; i < n; ++i) {
+        if ((L->profile >> i) & 1u)
+            MOE_CUDA(cudaEventElapsedTime(&stage_ms[i], L->ev[i], L->ev[i + 1]), "elapsed");
+        else
+            stage_ms[i] = -1.0f;
+    }
     return MOE_OK;
 }
 

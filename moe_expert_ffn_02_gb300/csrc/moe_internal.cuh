@@ -159,7 +159,7 @@ struct moe_layer {
     float* router_b;       // [E] (zeros when no bias)
     uint32_t* dev_status;  // device status word
     uint32_t wait_limit;
-    bool profile;          // record stage events in forward calls
+    uint32_t profile;      // stages whose events forward calls record (bit s: stage s), 0 = off
     cudaEvent_t ev[MOE_PROFILE_STAGES + 1];
     cudaStream_t ev_stream;
 };

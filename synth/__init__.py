@@ -140,6 +140,8 @@ WORKLOADS = {
                                  description="DeepSeek-V3 expert shapes, 32 experts, T=1024 (profiling)"),
     "ds_decode_probe": Workload("ds_decode_probe", 16, 7168, 2048, 32, 8,
                                 description="DeepSeek-V3 expert shapes, 32 experts, T=16 (profiling)"),
+    "ds_decode_t1_probe": Workload("ds_decode_t1_probe", 1, 7168, 2048, 32, 8,
+                                   description="DeepSeek-V3 expert shapes, 32 experts, T=1 (profiling)"),
 }
 
 

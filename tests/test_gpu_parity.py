@@ -163,6 +163,29 @@ def test_host_entry_matches_device_entry(h):
     layer.close()
 
 
+def test_profile_selects_stages_and_changes_no_result(h):
+    """The measurement hook times every stage, or only the selected ones
+    (the others read -1), and the layer output is the same either way."""
+    import moe_expert_ffn_02_gb300 as moe
+    wl = small_wl(16, 4, H=384, I=256, T=50)
+    inp = synth.make_inputs(wl, seed=12)
+    layer = h.make_layer(wl, inp)
+    y0, _ = h.run_forward(layer, inp["x"], 2, want_dbg=False)
+    for stages in (None, ("gate_up",), ("route", "down")):
+        moe.moe_profile_enable(layer.handle, True, stages=stages)
+        y1, _ = h.run_forward(layer, inp["x"], 2, want_dbg=False)
+        ms = moe.moe_profile_read(layer.handle)
+        timed = set(moe.PROFILE_STAGES if stages is None else stages)
+        for name, v in ms.items():
+            assert (v >= 0.0) if name in timed else (v == -1.0), (stages, ms)
+        assert np.array_equal(y1, y0)
+        moe.moe_profile_enable(layer.handle, False)
+    for bad in (moe.PROFILE_SELECT, 7, moe.PROFILE_SELECT | 0x40):   # no stage; no selector; unknown stage
+        with pytest.raises(moe.MoeError):
+            moe._check(moe.load().moe_profile_enable(layer.handle, bad))
+    layer.close()
+
+
 def test_bounded_wait_reports_timeout_without_fault(h):
     import moe_expert_ffn_02_gb300 as moe
     wl = synth.WORKLOADS["tiny"]
