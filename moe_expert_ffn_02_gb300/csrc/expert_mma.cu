@@ -338,12 +338,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_gemm_kernel(ExpertArgs a) 
 template <bool GU>
 static cudaError_t launch_expert(const moe_layer* L, const WsLayout& lay, char* ws, cudaStream_t s) {
     using C = Cfg<GU>;
-    static bool attr_set[2] = {false, false};
-    if (!attr_set[GU]) {
-        cudaError_t e = cudaFuncSetAttribute(expert_gemm_kernel<GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::SMEM + 1024);
+    {
+        cudaError_t e = ensure_smem_limit<expert_gemm_kernel<GU>>(C::SMEM + 1024);
         if (e != cudaSuccess) return e;
-        attr_set[GU] = true;
     }
     ExpertArgs a;
     const int H = L->d.hidden, I = L->d.inter;

@@ -365,12 +365,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
 
 template <bool GU>
 static cudaError_t launch(const moe_layer* L, const WsLayout& lay, char* ws, cudaStream_t s) {
-    static bool attr[2] = {false, false};
-    if (!attr[GU]) {
-        cudaError_t e =
-            cudaFuncSetAttribute(expert_tc_kernel<GU>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM + 1024);
+    {
+        cudaError_t e = ensure_smem_limit<expert_tc_kernel<GU>>(SMEM + 1024);
         if (e != cudaSuccess) return e;
-        attr[GU] = true;
     }
     Args a;
     const int H = L->d.hidden, I = L->d.inter;

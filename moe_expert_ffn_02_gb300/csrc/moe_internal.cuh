@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -310,6 +312,22 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(
 
 // Launchers (defined in the .cu files, called from api.cu).
 namespace moe {
+
+// Raise a kernel's dynamic shared-memory limit to `bytes`, once per device:
+// the attribute belongs to the device current when it is set, so a process
+// that drives layers on several devices sets it on each of them.
+template <auto Kernel>
+cudaError_t ensure_smem_limit(int bytes) {
+    static std::atomic<uint64_t> done{0};     // bit d: set on device d (< 64)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
 
 // Launch with programmatic stream serialisation (see pdl_wait).
 template <typename... KArgs, typename... Args>

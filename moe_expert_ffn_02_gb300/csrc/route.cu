@@ -103,12 +103,9 @@ cudaError_t launch_router_logits(const moe_layer* L, const uint16_t* x, int T, f
         const int slice = H / ksplit;
         const int tc = max(1, min(GEMV_TC, (160 * 1024) / (slice * 2)));
         const size_t smem = (size_t)tc * slice * 2;
-        static bool attr = false;
-        if (!attr) {
-            cudaError_t e = cudaFuncSetAttribute(router_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 160 * 1024 + 4096);
+        {
+            cudaError_t e = ensure_smem_limit<router_gemv_kernel>(160 * 1024 + 4096);
             if (e != cudaSuccess) return e;
-            attr = true;
         }
         dim3 grid((E + GEMV_WARPS - 1) / GEMV_WARPS, ksplit);
         return launch_pdl(router_gemv_kernel, grid, dim3(GEMV_WARPS * 32), smem, s, x, L->router_w, T, H, E, slice, tc,

@@ -251,11 +251,9 @@ cudaError_t launch_router_tc(const moe_layer* L, const uint16_t* x, int T, float
     const int H = L->d.hidden, E = L->d.n_experts;
     rt::EncodeTiled enc = rt::encoder();
     if (!enc) return cudaErrorNotSupported;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(rt::router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, rt::SMEM);
+    {
+        cudaError_t e = ensure_smem_limit<rt::router_tc_kernel>(rt::SMEM);
         if (e != cudaSuccess) return e;
-        attr = true;
     }
     CUtensorMap tx, tw;
     {
