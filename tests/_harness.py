@@ -111,6 +111,26 @@ def assert_routing_equal(got: dict, ref: dict):
     assert np.array_equal(got["inv_row"], ref["inv_row"]), "inv_row differs"
 
 
+def count_routing_switches(gpu_ids: np.ndarray, L_oracle: np.ndarray, k: int) -> int:
+    """Route the oracle on its own fp32 logits (an independent run, not the
+    GPU's logits) and compare the ordered top-k with the GPU's.  Every token
+    whose routing differs must be a near-tie: at the first rank where the two
+    lists part, the oracle's logit of its expert exceeds that of the GPU's
+    by at most the sum of the two logits' tolerances, 2e-5 * (1 + |L|)
+    (both sides are within 1e-5 * (1 + |L|) of the exact logit, which the
+    tests assert separately).  Returns the number of such tokens."""
+    import oracle
+    ref = oracle.route_from_logits(L_oracle, k)["ids"]
+    diff = np.nonzero((ref != gpu_ids).any(axis=1))[0]
+    for t in diff:
+        p = int(np.nonzero(ref[t] != gpu_ids[t])[0][0])
+        a, b = int(ref[t, p]), int(gpu_ids[t, p])
+        la, lb = float(L_oracle[t, a]), float(L_oracle[t, b])
+        assert 0.0 <= la - lb <= 2e-5 * (1.0 + max(abs(la), abs(lb))), (int(t), p, a, b, la, lb)
+    print(f"[routing] tokens routed differently under the oracle's own logits: {len(diff)} of {len(ref)}")
+    return len(diff)
+
+
 REL_L2_TOL = 5e-3          # relative L2 error of y
 MAX_ABS_TOL = 3e-2         # max abs error / rms(y_oracle)
 

@@ -55,6 +55,7 @@ def test_router_logits_tolerance_and_routing(h):
     Lref = oracle.logits(inp["x"], inp["router_w"], inp["router_b"])
     assert np.all(np.abs(got["logits"] - Lref) <= 1e-5 * (1 + np.abs(Lref)))
     h.assert_routing_equal(got, oracle.route_from_logits(got["logits"], wl.top_k))
+    h.count_routing_switches(got["topk_ids"], Lref, wl.top_k)
     layer.close()
 
 
@@ -251,6 +252,7 @@ def test_deepseek_decode_layer(h, ds_inputs, name):
     assert np.all(np.abs(r["logits"] - Lref) <= 1e-5 * (1 + np.abs(Lref)))
     ref_route = oracle.route_from_logits(r["logits"], wl.top_k)
     h.assert_routing_equal(dbg, ref_route)
+    h.count_routing_switches(r["topk_ids"], Lref, wl.top_k)
     xq, sx = oracle.quant_1x128(synth.bf16_to_f32(inp["x"]))
     assert np.array_equal(dbg["xq"], xq) and np.array_equal(dbg["sx"], sx)
     h.check_layer_output(inp, wl.top_k, dbg, y)
@@ -280,6 +282,7 @@ def test_deepseek_prefill_layers_sampled(h, ds_inputs, name):
     sub = np.sort(rows)
     Lref = oracle.logits(inp["x"][sub], inp["router_w"], inp["router_b"])
     assert np.all(np.abs(r["logits"][sub] - Lref) <= 1e-5 * (1 + np.abs(Lref)))
+    h.count_routing_switches(r["topk_ids"][sub], Lref, wl.top_k)
     xq, sx = oracle.quant_1x128(synth.bf16_to_f32(inp["x"][sub]))
     assert np.array_equal(dbg["xq"][sub], xq) and np.array_equal(dbg["sx"][sub], sx)
     h.check_layer_output(inp, wl.top_k, dbg, y, rows=sub)
@@ -295,5 +298,8 @@ def test_kimi_prefill_layer_sampled(h):
     ref_route = oracle.route_from_logits(r["logits"], wl.top_k)
     h.assert_routing_equal(dbg, ref_route)
     rows = sample_rows(wl.T, ref_route, n_rand=32)
+    Lref = oracle.logits(inp["x"][rows], inp["router_w"], inp["router_b"])
+    assert np.all(np.abs(r["logits"][rows] - Lref) <= 1e-5 * (1 + np.abs(Lref)))
+    h.count_routing_switches(r["topk_ids"][rows], Lref, wl.top_k)
     h.check_layer_output(inp, wl.top_k, dbg, y, rows=rows)
     layer.close()
