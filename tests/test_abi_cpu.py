@@ -89,3 +89,35 @@ def test_null_handle_calls_fail_cleanly(lib):
     assert lib.moe_route(None, None, 0, None, None, 0, None) == 1
     assert lib.moe_destroy(None) == 1
     assert moe.moe_status_string(3) == "MOE_ERR_WORKSPACE"
+
+
+def test_plain_c_caller_compiles_links_and_gets_a_status(lib, tmp_path):
+    """The boundary is a C ABI: a C99 program (no C++, no CUDA headers)
+    includes include/moe.h with every warning an error, links libmoe.so and
+    gets a status and a message back for a rejected call."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "caller.c"
+    src.write_text(
+        '#include <stdio.h>\n#include "moe.h"\n'
+        "int main(void) {\n"
+        "    moe_desc d = {0};\n"
+        "    moe_layer* layer = 0;\n"
+        "    d.hidden = 256; d.inter = 256; d.n_experts = 8; d.top_k = 2; d.n_shared = 1; d.shared_inter = 256;\n"
+        "    moe_status st = moe_create(&d, 0, 0, &layer);\n"
+        '    printf("%d|%s|%s\\n", (int)st, moe_status_string(st), moe_last_error());\n'
+        "    return layer != 0;\n"
+        "}\n")
+    exe = tmp_path / "caller"
+    libdir = os.path.dirname(moe.library_path())
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-L", libdir, "-lmoe", f"-Wl,-rpath,{libdir}", "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    code, name, msg = r.stdout.strip().split("|", 2)
+    assert int(code) == 1 and name == "MOE_ERR_INVALID_ARG" and msg
