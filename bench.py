@@ -96,8 +96,12 @@ def metric_of(wl):
 
 
 def value_of(wl, seconds_per_step: float, n_ranks: int = 1):
+    """Whole-job figure of a step timed as the max over n_ranks replicas, each
+    running the workload's layer: decode, microseconds per layer over all the
+    layers the job ran (n_ranks per step); prefill, tokens per second over all
+    ranks."""
     if is_decode(wl):
-        return seconds_per_step * 1e6
+        return seconds_per_step * 1e6 / n_ranks
     return wl.T * n_ranks / seconds_per_step
 
 

@@ -106,3 +106,34 @@ def test_bench_reference_arm_prints_the_contract_line():
     env = dict(os.environ, RANK="1", WORLD_SIZE="2")
     out = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=root, env=env)
     assert out.returncode == 0 and not [l for l in out.stdout.splitlines() if l.startswith("{")]
+
+
+def test_bench_metric_helpers():
+    """The bench line's value and CPU-baseline arithmetic, and the rule that
+    the roofline's traffic figure is used only for the sources it was taken on."""
+    import json
+    import os
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    sys.path.insert(0, root)
+    import bench
+    dec, pre = synth.WORKLOADS["ds_decode_t16"], synth.WORKLOADS["ds_prefill_8k"]
+    assert bench.metric_of(dec) == ("moe_layer_decode_us_per_layer", "us/layer", False)
+    assert bench.metric_of(pre) == ("moe_layer_prefill_tokens_per_s", "tokens/s", True)
+    # one replica: the step time itself / T tokens per step time; N replicas: the whole job
+    assert bench.value_of(dec, 764e-6) == 764e-6 * 1e6
+    assert abs(bench.value_of(dec, 800e-6, 4) - 200.0) < 1e-9
+    assert abs(bench.value_of(pre, 4e-3) - 8192 / 4e-3) < 1e-6
+    assert abs(bench.value_of(pre, 4e-3, 2) - 2 * 8192 / 4e-3) < 1e-6
+    # oracle sample scaled to the workload's unit
+    assert abs(bench.cpu_value(dec, 2.0, 4) - 2.0 / 4 * 16 * 1e6) < 1e-3
+    assert abs(bench.cpu_value(pre, 2.0, 100) - 50.0) < 1e-12
+    # traffic: only when the committed capture was taken on the current kernel sources
+    h = bench.kernel_source_hash()
+    assert h == bench.kernel_source_hash() and len(h) == 16
+    d = json.load(open(bench.TRAFFIC_FILE))
+    for wl_name, per in d.items():
+        for kernel, e in per.items():
+            got = bench.traffic_for(kernel, wl_name)
+            assert got == (e["dram_bytes_per_launch"] if e["source_hash"] == h else None)
+    assert bench.traffic_for("gate_up", "no_such_workload") is None
