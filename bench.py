@@ -522,7 +522,7 @@ def run_layers(a, wl):
         "config": {"workload": wl.name, "T": T, "hidden": H, "inter": wl.inter, "n_experts": wl.n_experts,
                    "top_k": wl.top_k, "n_shared": wl.n_shared, "parallelism": "replicas1", "layers": a.layers,
                    "graph": True, "l2": "flushed between steps (512 MiB write, outside the timed events)"},
-        "roofline": roof, "cpu_baseline": None, "e2e": None, "gpu_launches": 9 * a.layers * a.steps,
+        "roofline": roof, "cpu_baseline": None, "e2e": None, "gpu_launches": (6 if T <= 64 else 9) * a.layers * a.steps,
         "clocks": clk.summary(),
     }
     if a.host_tiles:
