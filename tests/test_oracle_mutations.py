@@ -4,7 +4,8 @@ mistake in a copy of oracle.c (on the CPU), and the pin suite
 the kind a reader checking the oracle against the pages would look for:
 gate and up swapped, the bias subtracted, the tie-break reversed, a
 coefficient of the gate-weight exp wrong, a block-scale index transposed,
-the gate weight left out of the combine."""
+the gate weight or the shared expert left out of the combine, E4M3 or bf16
+rounding that truncates, an activation scale off by one step."""
 import os
 import shutil
 import subprocess
@@ -25,6 +26,12 @@ MUTATIONS = {
         "g += pg * ((double)ev->sg[(int64_t)kb * IB + (i / QBLOCK)] * (double)sx[kb]);"),
     "gate_weight_dropped": ("for (int32_t h = 0; h < H; ++h) acc[h] += wj * o[h];",
                             "for (int32_t h = 0; h < H; ++h) acc[h] += o[h];"),
+    "e4m3_truncates": ("double m = nearbyint((ldexp(a, -E) - 1.0) * 8.0);",
+                       "double m = floor((ldexp(a, -E) - 1.0) * 8.0);"),
+    "quant_scale_off": ("? amax / 448.0f : 1.0f;", "? amax / 447.0f : 1.0f;"),
+    "shared_expert_dropped": ("for (int32_t h = 0; h < H; ++h) acc[h] = o[h];",
+                              "for (int32_t h = 0; h < H; ++h) acc[h] = 0.0 * o[h];"),
+    "bf16_output_truncates": ("double r = nearbyint(a / ulp) * ulp;", "double r = floor(a / ulp) * ulp;"),
 }
 
 
