@@ -48,6 +48,10 @@
  *  - Limits: hidden and inter multiples of 128; 1 <= top_k <= 32;
  *    top_k <= n_experts <= 1024; shared_inter == inter; T*top_k < 2^31.
  *    x, y and all weight pointers 16-byte aligned; workspace 256-byte aligned.
+ *  - Devices: a layer lives on the device that was current at moe_create.
+ *    Every call that enqueues work must be made with that device current;
+ *    otherwise it returns MOE_ERR_INVALID_ARG before enqueuing anything.
+ *    moe_destroy selects the layer's device itself.
  *  - Thread safety: one handle may be used by one stream at a time; separate
  *    handles are independent.
  */
@@ -74,7 +78,10 @@ typedef enum {
     MOE_ERR_TIMEOUT = 6          /* a kernel wait gave up (device word)        */
 } moe_status;
 
-/* Bits of the device status word (moe_get_device_status). */
+/* Bits of the device status word (moe_get_device_status).  The kernels
+ * check every expert id and every permuted row they index with; a bad one
+ * sets its bit and is clamped (ids) or skipped (rows), so no access leaves
+ * the buffers.  The results of that call are then undefined. */
 #define MOE_DEV_BAD_EXPERT_ID  0x1u   /* a routing id outside [0, n_experts)  */
 #define MOE_DEV_BAD_ROW        0x2u   /* a permutation row outside its range  */
 #define MOE_DEV_WAIT_TIMEOUT   0x4u   /* a pipeline wait hit its limit        */
@@ -189,8 +196,12 @@ moe_status moe_route_from_logits(moe_layer* layer, const float* logits, int32_t 
  * C callers without an allocator to carve a workspace from.
  * Its scratch is a fixed array of MOE_NOALLOC_SCRATCH_BYTES (4 MiB) compiled
  * into the library; every GPU that loads the library holds it until the
- * process exits.  Outputs go to `out` exactly as moe_route_from_logits
- * writes them (same kernels, bit-identical results).
+ * process exits.  Outputs go to `out` bit for bit as moe_route_from_logits
+ * writes them (for decode-sized batches the workspace entry fuses the
+ * stages into one kernel and this entry runs them one by one; both call
+ * the same device functions, so the results are identical).
+ *  - Device: the layer's device must be current (MOE_ERR_INVALID_ARG
+ *    otherwise).
  *  - Size limit: the routing scratch for (T, n_experts, top_k) must fit the
  *    array -- roughly 160 bytes per token at E = 256, k = 8 (T <= ~26,000) --
  *    otherwise MOE_ERR_UNSUPPORTED is returned and nothing runs.
@@ -285,6 +296,18 @@ moe_status moe_set_wait_limit(moe_layer* layer, uint32_t microseconds);
 /* Test hook: run one bounded wait on an mbarrier that is never signalled,
  * so the timeout path can be exercised without a fault. */
 moe_status moe_debug_timeout_probe(moe_layer* layer, void* stream);
+
+/* Test hook (fault injection, host side): the next call on this layer that
+ * routes (MOE_DEV_BAD_EXPERT_ID) or runs a forward entry (MOE_DEV_BAD_ROW)
+ * overwrites one word of its own workspace -- the expert id of (token 0,
+ * slot 0) with n_experts + 3, or the internal row of (token 0, slot 0) with
+ * a row past the permuted buffers -- before the kernels that read it.
+ * Those kernels must flag it in the device status word and clamp or skip
+ * it, so nothing reads or writes outside the buffers; the call's outputs
+ * are then undefined and moe_get_device_status returns
+ * MOE_ERR_DEVICE_CHECK.  Each planted fault fires once.  Other bits:
+ * MOE_ERR_INVALID_ARG. */
+moe_status moe_debug_inject(moe_layer* layer, uint32_t faults);
 
 /* Measurement hook.  With profiling enabled, every forward call records a
  * CUDA event on its stream at the boundaries of the timed stages:

@@ -21,7 +21,7 @@ __all__ = [
     "MoeError", "MoeDesc", "MoeWeights", "MoeRouteOut", "MODE_ROUTE", "MODE_PREFILL", "MODE_DECODE",
     "DECODE_MAX_T", "moe_create", "moe_destroy", "moe_workspace_bytes", "moe_route", "moe_route_from_logits",
     "moe_route_from_logits_noalloc", "moe_forward_prefill", "moe_forward_decode", "moe_forward_host", "moe_get_device_status",
-    "moe_set_wait_limit", "moe_debug_timeout_probe", "moe_profile_enable", "moe_profile_read", "moe_status_string", "moe_last_error",
+    "moe_set_wait_limit", "moe_debug_timeout_probe", "moe_debug_inject", "moe_profile_enable", "moe_profile_read", "moe_status_string", "moe_last_error",
     "moe_abi_version", "moe_forward_smallep", "moe_forward_deferred", "moe_layers_workspace_bytes",
     "moe_forward_layers", "smallep_groups", "moe_create_ex", "moe_tiles_bytes", "moe_tiles_load", "moe_forward_tiles",
     "CREATE_HOST_TILES", "library_path", "load", "Layer", "LayerStackGraph", "StreamedStack",
@@ -93,6 +93,7 @@ def load(build_if_missing: bool = False):
             "moe_get_device_status": ([vp, vp, ctypes.POINTER(u32)], st),
             "moe_set_wait_limit": ([vp, u32], st),
             "moe_debug_timeout_probe": ([vp, vp], st),
+            "moe_debug_inject": ([vp, u32], st),
             "moe_route_from_logits_noalloc": ([vp, vp, i32, ctypes.POINTER(MoeRouteOut), vp], st),
             "moe_forward_smallep": ([vp, i32, i32, vp, i32, vp, vp, sz, vp], st),
             "moe_create_ex": ([ctypes.POINTER(MoeDesc), ctypes.POINTER(MoeWeights), u32, vp, ctypes.POINTER(vp)], st),
@@ -255,6 +256,13 @@ def moe_set_wait_limit(layer: int, microseconds: int) -> None:
 
 def moe_debug_timeout_probe(layer: int, stream: int = 0) -> None:
     _check(load().moe_debug_timeout_probe(layer, stream))
+
+
+def moe_debug_inject(layer: int, faults: int) -> None:
+    """Plant the faults (DEV_BAD_EXPERT_ID | DEV_BAD_ROW) in the next routing
+    or forward call's workspace; the kernels must flag them and stay in
+    bounds (test hook, see include/moe.h)."""
+    _check(load().moe_debug_inject(layer, faults))
 
 
 PROFILE_STAGES = ("route", "quant_x", "gate_up", "down", "combine")

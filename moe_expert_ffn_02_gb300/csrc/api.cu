@@ -3,6 +3,7 @@
 #include "moe_internal.cuh"
 
 #include <algorithm>
+#include <cstddef>
 #include <cstdarg>
 #include <cstdio>
 #include <string>
@@ -37,7 +38,7 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 inline size_t up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 constexpr uint32_t kDefaultWaitLimitUs = 2000000u;   // 2 s per bounded wait
-constexpr int kBN = 64;                              // n tile of the expert GEMMs
+constexpr int kBN = moe::DEC_TILE_N;                 // n tile of the weight-streaming expert GEMMs
 
 moe::WsLayout make_layout(const moe_layer* L, int T, int mode) {
     moe::WsLayout l{};
@@ -76,14 +77,35 @@ moe::WsLayout make_layout(const moe_layer* L, int T, int mode) {
     return l;
 }
 
+// The host-side tests build a stand-in handle whose recorded device differs
+// from the current one; they rely on `device` following the descriptor.
+static_assert(offsetof(moe_layer, device) == sizeof(moe_desc), "moe_layer: device must follow the descriptor");
+
 moe_status check_layer(const moe_layer* L) {
     if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
     return MOE_OK;
 }
 
+// Every entry that enqueues work checks that the calling thread's current
+// device is the one the layer lives on: a kernel launched on another device
+// would dereference this layer's weights and workspace from the wrong GPU.
+moe_status check_device(const moe_layer* L) {
+    int cur = -1;
+    cudaError_t e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (cur != L->device)
+        return fail(MOE_ERR_INVALID_ARG, "the current device (%d) is not the layer's device (%d)", cur, L->device);
+    return MOE_OK;
+}
+
+moe_status check_layer_device(const moe_layer* L) {
+    moe_status st = check_layer(L);
+    return st != MOE_OK ? st : check_device(L);
+}
+
 moe_status check_call(moe_layer* L, int T, int mode, const void* x, const void* y, void* ws, size_t ws_bytes,
                       moe::WsLayout* lay) {
-    moe_status st = check_layer(L);
+    moe_status st = check_layer_device(L);
     if (st == MOE_OK && mode != MOE_MODE_ROUTE && L->tiles_host && !L->w_gu)
         return fail(MOE_ERR_INVALID_ARG, "the layer keeps its tiles in host memory: run it with moe_forward_tiles");
     if (st != MOE_OK) return st;
@@ -112,8 +134,10 @@ moe_status run_route(moe_layer* L, const uint16_t* x, const float* logits_in, in
     const int k = L->d.top_k;
     int32_t* ids = reinterpret_cast<int32_t*>(ws + lay.ids);
     float* w = reinterpret_cast<float*>(ws + lay.w);
-    // a decode-sized batch: top-k and grouping in one single-CTA kernel
-    const bool small = lay.n_chunks == 1 && L->d.n_experts <= 512;
+    // a decode-sized batch: top-k and grouping in one single-CTA kernel (not when a bad expert id is to be
+    // planted between the two)
+    const bool plant_id = (L->inject & MOE_DEV_BAD_EXPERT_ID) != 0;
+    const bool small = lay.n_chunks == 1 && L->d.n_experts <= 512 && !plant_id;
     if (small) {
         const float* part = logits_in ? logits_in : reinterpret_cast<const float*>(ws + lay.logit_part);
         if (!logits_in)
@@ -140,6 +164,10 @@ moe_status run_route(moe_layer* L, const uint16_t* x, const float* logits_in, in
         MOE_CUDA(moe::launch_topk(L, part, lay.ksplit, true, T, dbg ? dbg->logits : nullptr, ids,
                                   w, s),
                  "top-k");
+    }
+    if (plant_id) {                   // moe_debug_inject: an expert id outside [0, E) for (token 0, slot 0)
+        MOE_CUDA(moe::launch_plant(ids, L->d.n_experts + 3, s), "fault injection");
+        L->inject &= ~(uint32_t)MOE_DEV_BAD_EXPERT_ID;
     }
     if (dbg && dbg->topk_ids)
         MOE_CUDA(cudaMemcpyAsync(dbg->topk_ids, ids, sizeof(int32_t) * (size_t)T * k, cudaMemcpyDeviceToDevice, s),
@@ -190,6 +218,11 @@ moe_status run_forward(moe_layer* L, int mode, const uint16_t* x, int T, uint16_
     MOE_CUDA(mark(0), "profile event");
     st = run_route(L, x, nullptr, T, lay, ws, dbg, s, tc_path ? moe::tc_tile_n() : kBN);
     if (st != MOE_OK) return st;
+    if (L->inject & MOE_DEV_BAD_ROW) {   // moe_debug_inject: an internal row outside the workspace for (0, 0)
+        MOE_CUDA(moe::launch_plant(reinterpret_cast<int32_t*>(ws + lay.inv_int), lay.rows_pad + 5, s),
+                 "fault injection");
+        L->inject &= ~(uint32_t)MOE_DEV_BAD_ROW;
+    }
     MOE_CUDA(mark(1), "profile event");
     MOE_CUDA(moe::launch_quant_scatter(L, x, T, lay, ws, dbg ? dbg->xq : nullptr, dbg ? dbg->sx : nullptr, s),
              "activation quantisation");
@@ -333,7 +366,7 @@ MOE_EXPORT moe_status moe_tiles_bytes(moe_layer* L, size_t* bytes) {
 }
 
 MOE_EXPORT moe_status moe_tiles_load(moe_layer* L, void* slot, void* stream) {
-    moe_status st = check_layer(L);
+    moe_status st = check_layer_device(L);
     if (st != MOE_OK) return st;
     if (!L->tiles_host) return fail(MOE_ERR_INVALID_ARG, "the layer keeps its tiles on the device");
     if (!slot || !aligned(slot, 256)) return fail(MOE_ERR_INVALID_ARG, "slot NULL or not 256-byte aligned");
@@ -345,7 +378,7 @@ MOE_EXPORT moe_status moe_tiles_load(moe_layer* L, void* slot, void* stream) {
 
 MOE_EXPORT moe_status moe_forward_tiles(moe_layer* L, int32_t mode, const void* slot, const uint16_t* x, int32_t T,
                                         uint16_t* y, void* ws, size_t ws_bytes, void* stream) {
-    moe_status st = check_layer(L);
+    moe_status st = check_layer_device(L);
     if (st != MOE_OK) return st;
     if (mode != MOE_MODE_PREFILL && mode != MOE_MODE_DECODE) return fail(MOE_ERR_INVALID_ARG, "mode must be 1 or 2");
     if (!L->tiles_host) return fail(MOE_ERR_INVALID_ARG, "the layer keeps its tiles on the device");
@@ -360,13 +393,20 @@ MOE_EXPORT moe_status moe_forward_tiles(moe_layer* L, int32_t mode, const void* 
 
 MOE_EXPORT moe_status moe_destroy(moe_layer* L) {
     if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
-    cudaError_t e = cudaDeviceSynchronize();
+    // release on the layer's own device, whichever device the caller has current
+    int cur = -1;
+    cudaError_t e = cudaGetDevice(&cur);
+    if (e == cudaSuccess && cur != L->device) e = cudaSetDevice(L->device);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_destroy: selecting the layer's device");
+    e = cudaDeviceSynchronize();
     if (L->profile)
         for (cudaEvent_t ev : L->ev) cudaEventDestroy(ev);
     if (L->tiles_host) cudaFreeHost(L->tiles_host);
     cudaFree(L->w_gu); cudaFree(L->w_dn); cudaFree(L->s_gu); cudaFree(L->s_dn); cudaFree(L->r_gu); cudaFree(L->r_dn);
     cudaFree(L->router_w); cudaFree(L->router_w3); cudaFree(L->router_b); cudaFree(L->dev_status);
+    const int dev = L->device;
     delete L;
+    if (cur >= 0 && cur != dev) cudaSetDevice(cur);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_destroy synchronise");
 }
 
@@ -497,7 +537,7 @@ MOE_EXPORT moe_status moe_forward_layers(moe_layer* const* layers, int32_t n_lay
 
 MOE_EXPORT moe_status moe_forward_host(moe_layer* L, int32_t mode, const uint16_t* x_host, int32_t T,
                                        uint16_t* y_host, void* ws, size_t ws_bytes, void* stream) {
-    moe_status st = check_layer(L);
+    moe_status st = check_layer_device(L);
     if (st != MOE_OK) return st;
     if (mode != MOE_MODE_PREFILL && mode != MOE_MODE_DECODE) return fail(MOE_ERR_INVALID_ARG, "mode must be 1 or 2");
     if (T < 0 || (T > 0 && (!x_host || !y_host))) return fail(MOE_ERR_INVALID_ARG, "bad host buffers or T");
@@ -520,7 +560,7 @@ MOE_EXPORT moe_status moe_forward_host(moe_layer* L, int32_t mode, const uint16_
 }
 
 MOE_EXPORT moe_status moe_get_device_status(moe_layer* L, void* stream, uint32_t* flags) {
-    moe_status st = check_layer(L);
+    moe_status st = check_layer_device(L);
     if (st != MOE_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint32_t v = 0;
@@ -542,7 +582,7 @@ MOE_EXPORT moe_status moe_set_wait_limit(moe_layer* L, uint32_t limit) {
 }
 
 MOE_EXPORT moe_status moe_profile_enable(moe_layer* L, int32_t enable) {
-    moe_status st = check_layer(L);
+    moe_status st = check_layer_device(L);
     if (st != MOE_OK) return st;
     const uint32_t all = (1u << MOE_PROFILE_STAGES) - 1u;
     uint32_t mask = 0;
@@ -584,8 +624,18 @@ MOE_EXPORT moe_status moe_profile_read(moe_layer* L, float* stage_ms, int32_t n)
 }
 
 MOE_EXPORT moe_status moe_debug_timeout_probe(moe_layer* L, void* stream) {
-    moe_status st = check_layer(L);
+    moe_status st = check_layer_device(L);
     if (st != MOE_OK) return st;
     MOE_CUDA(moe::launch_timeout_probe(L, static_cast<cudaStream_t>(stream)), "timeout probe");
+    return MOE_OK;
+}
+
+MOE_EXPORT moe_status moe_debug_inject(moe_layer* L, uint32_t faults) {
+    moe_status st = check_layer(L);
+    if (st != MOE_OK) return st;
+    if (faults & ~(uint32_t)(MOE_DEV_BAD_EXPERT_ID | MOE_DEV_BAD_ROW))
+        return fail(MOE_ERR_INVALID_ARG, "only MOE_DEV_BAD_EXPERT_ID and MOE_DEV_BAD_ROW can be planted (got %#x)",
+                    faults);
+    L->inject |= faults;
     return MOE_OK;
 }

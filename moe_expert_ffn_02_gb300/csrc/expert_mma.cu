@@ -36,7 +36,7 @@
 
 namespace moe {
 
-constexpr int BN = 64;                  // rows (tokens) per n tile
+constexpr int BN = DEC_TILE_N;          // rows (tokens) per n tile
 constexpr int CW = 8;                   // consumer warps (16 output rows each)
 constexpr int NTHREADS = (CW + 1) * 32; // + producer warp
 constexpr int XSTRIDE = 128;            // activation row in shared memory (swizzled)
@@ -387,15 +387,19 @@ cudaError_t launch_expert_down(const moe_layer* L, int T, const WsLayout& lay, c
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ O, const int32_t* __restrict__ inv_int,
                                                       const float* __restrict__ w, const int32_t* __restrict__ offsets_pad,
-                                                      int T, int H, int k, int E, int n_shared,
-                                                      uint16_t* __restrict__ y) {
+                                                      int T, int H, int k, int E, int n_shared, int ld,
+                                                      uint16_t* __restrict__ y, uint32_t* status) {
     __shared__ int rows[MAX_TOPK];
     __shared__ float wt[MAX_TOPK];
     const int t = blockIdx.x;
     pdl_trigger();
     pdl_wait();
     if (threadIdx.x < k) {
-        rows[threadIdx.x] = inv_int[(size_t)t * k + threadIdx.x];
+        // a row outside the expert outputs is flagged and its slot left out (never read)
+        const int row = inv_int[(size_t)t * k + threadIdx.x];
+        const bool ok = row >= 0 && row < ld;
+        if (!ok && blockIdx.y == 0) atomicOr(status, MOE_DEV_BAD_ROW);
+        rows[threadIdx.x] = ok ? row : -1;
         wt[threadIdx.x] = w[(size_t)t * k + threadIdx.x];
     }
     __syncthreads();
@@ -403,6 +407,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     for (int c = (blockIdx.y * blockDim.x + threadIdx.x) * 4; c < H; c += gridDim.y * blockDim.x * 4) {
         float4 acc = n_shared ? *reinterpret_cast<const float4*>(O + shrow * H + c) : make_float4(0.f, 0.f, 0.f, 0.f);
         for (int j = 0; j < k; ++j) {
+            if (rows[j] < 0) continue;
             const float4 o = *reinterpret_cast<const float4*>(O + (size_t)rows[j] * H + c);
             const float wj = wt[j];
             acc.x = __fmaf_rn(wj, o.x, acc.x);
@@ -427,7 +432,7 @@ cudaError_t launch_combine(const moe_layer* L, int T, const WsLayout& lay, char*
                                      reinterpret_cast<const int32_t*>(ws + lay.inv_int),
                                      reinterpret_cast<const float*>(ws + lay.w),
                                      reinterpret_cast<const int32_t*>(ws + lay.offsets_pad), T, L->d.hidden, L->d.top_k,
-                                     L->d.n_experts, L->d.n_shared, y);
+                                     L->d.n_experts, L->d.n_shared, lay.rows_pad, y, L->dev_status);
 }
 
 // ---------------------------------------------------------------------------
@@ -453,8 +458,9 @@ __global__ void __launch_bounds__(256) combine_split_kernel(const float* __restr
                                                             const float* __restrict__ w,
                                                             const int32_t* __restrict__ offsets_pad,
                                                             const uint8_t* __restrict__ defer, int T, int H, int k,
-                                                            int E, int n_shared, int n_ranks, uint16_t* __restrict__ y,
-                                                            uint16_t* __restrict__ y_next) {
+                                                            int E, int n_shared, int n_ranks, int ld,
+                                                            uint16_t* __restrict__ y, uint16_t* __restrict__ y_next,
+                                                            uint32_t* status) {
     __shared__ int rows[MAX_TOPK], part_of[MAX_TOPK];
     __shared__ float wt[MAX_TOPK];
     const int t = blockIdx.x;
@@ -462,7 +468,10 @@ __global__ void __launch_bounds__(256) combine_split_kernel(const float* __restr
     pdl_wait();
     if (threadIdx.x < k) {
         const int j = threadIdx.x;
-        rows[j] = inv_int[(size_t)t * k + j];
+        const int row = inv_int[(size_t)t * k + j];
+        const bool ok = row >= 0 && row < ld;
+        if (!ok && blockIdx.y == 0) atomicOr(status, MOE_DEV_BAD_ROW);
+        rows[j] = ok ? row : -1;
         wt[j] = w[(size_t)t * k + j];
         if (defer) {
             part_of[j] = defer[(size_t)t * k + j] ? 1 : 0;
@@ -482,7 +491,7 @@ __global__ void __launch_bounds__(256) combine_split_kernel(const float* __restr
             float4 acc = (p == 0 && n_shared) ? *reinterpret_cast<const float4*>(O + shrow * H + c)
                                               : make_float4(0.f, 0.f, 0.f, 0.f);
             for (int j = 0; j < k; ++j) {
-                if (part_of[j] != p) continue;
+                if (part_of[j] != p || rows[j] < 0) continue;
                 const float4 o = *reinterpret_cast<const float4*>(O + (size_t)rows[j] * H + c);
                 const float wj = wt[j];
                 acc.x = __fmaf_rn(wj, o.x, acc.x);
@@ -522,7 +531,7 @@ cudaError_t launch_combine_split(const moe_layer* L, int T, const WsLayout& lay,
         reinterpret_cast<const float*>(ws + lay.o), reinterpret_cast<const int32_t*>(ws + lay.inv_int),
         reinterpret_cast<const int32_t*>(ws + lay.ids), reinterpret_cast<const float*>(ws + lay.w),
         reinterpret_cast<const int32_t*>(ws + lay.offsets_pad), defer, T, L->d.hidden, L->d.top_k, L->d.n_experts,
-        L->d.n_shared, n_ranks, y, y_next);
+        L->d.n_shared, n_ranks, lay.rows_pad, y, y_next, L->dev_status);
 }
 
 // ---------------------------------------------------------------------------
@@ -533,11 +542,16 @@ cudaError_t launch_combine_split(const moe_layer* L, int T, const WsLayout& lay,
 __global__ void __launch_bounds__(128) h_gather_kernel(const uint8_t* __restrict__ hq, const float* __restrict__ shT,
                                                        int ld, const int32_t* __restrict__ inv_int,
                                                        const int32_t* __restrict__ offsets_pad, int E, int k, int S,
-                                                       int I, uint8_t* __restrict__ hq_out, float* __restrict__ sh_out) {
+                                                       int I, uint8_t* __restrict__ hq_out, float* __restrict__ sh_out,
+                                                       uint32_t* status) {
     const int t = blockIdx.x;
     const int IB = I / QB;
     for (int slot = 0; slot < S; ++slot) {
         const int row = slot < k ? inv_int[(size_t)t * k + slot] : offsets_pad[E] + t;
+        if (row < 0 || row >= ld) {                     // flagged and skipped, never read
+            if (threadIdx.x == 0) atomicOr(status, MOE_DEV_BAD_ROW);
+            continue;
+        }
         const size_t rec = (size_t)t * S + slot;
         if (hq_out)
             for (int c = threadIdx.x; c < IB * 8; c += blockDim.x) {
@@ -558,7 +572,7 @@ cudaError_t launch_h_gather(const moe_layer* L, int T, const WsLayout& lay, char
                                       reinterpret_cast<const float*>(ws + lay.shT), lay.rows_pad,
                                       reinterpret_cast<const int32_t*>(ws + lay.inv_int),
                                       reinterpret_cast<const int32_t*>(ws + lay.offsets_pad), L->d.n_experts,
-                                      L->d.top_k, S, L->d.inter, hq_out, sh_out);
+                                      L->d.top_k, S, L->d.inter, hq_out, sh_out, L->dev_status);
     return cudaGetLastError();
 }
 
@@ -630,6 +644,15 @@ __global__ void timeout_probe_kernel(uint32_t* status, uint32_t limit) {
 
 cudaError_t launch_timeout_probe(const moe_layer* L, cudaStream_t s) {
     timeout_probe_kernel<<<1, 32, 0, s>>>(L->dev_status, L->wait_limit);
+    return cudaGetLastError();
+}
+
+// Fault injection (moe_debug_inject): overwrite one routing word in the
+// workspace with a value the checked kernels must flag and skip.
+__global__ void plant_kernel(int32_t* word, int32_t value) { *word = value; }
+
+cudaError_t launch_plant(int32_t* word, int32_t value, cudaStream_t s) {
+    plant_kernel<<<1, 1, 0, s>>>(word, value);
     return cudaGetLastError();
 }
 

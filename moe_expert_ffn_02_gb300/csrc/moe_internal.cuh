@@ -18,6 +18,8 @@ constexpr int MAX_TOPK = 32;
 constexpr int MAX_EXPERTS = 1024;
 constexpr int ROW_PAD = 256;          // spare rows after every permuted buffer
 constexpr int ROW_ALIGN = 8;          // each group's rows start on a multiple of 8
+constexpr int DEC_TILE_N = 64;        // token rows per group tile of the weight-streaming (decode) GEMMs;
+                                      // routing-only entries build their group table with it too
 
 // ---------------------------------------------------------------------------
 // Permuted activation buffers (x codes, h codes) use the same 128-byte
@@ -162,6 +164,7 @@ struct moe_layer {
     uint32_t* dev_status;  // device status word
     uint32_t wait_limit;
     uint32_t profile;      // stages whose events forward calls record (bit s: stage s), 0 = off
+    uint32_t inject;       // MOE_DEV_* bits of faults the next forward call plants (moe_debug_inject)
     cudaEvent_t ev[MOE_PROFILE_STAGES + 1];
     cudaStream_t ev_stream;
 };
@@ -375,5 +378,6 @@ cudaError_t launch_combine(const moe_layer* L, int T, const WsLayout& lay, char*
 cudaError_t launch_combine_split(const moe_layer* L, int T, const WsLayout& lay, char* ws, int n_ranks,
                                  const uint8_t* defer, uint16_t* y, uint16_t* y_next, cudaStream_t s);
 cudaError_t launch_timeout_probe(const moe_layer* L, cudaStream_t s);
+cudaError_t launch_plant(int32_t* word, int32_t value, cudaStream_t s);
 void set_last_error(const char* msg);   // message returned by moe_last_error()
 }  // namespace moe

@@ -574,14 +574,20 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __re
                                                             const int32_t* __restrict__ offsets_pad, int E,
                                                             uint8_t* __restrict__ xp, float* __restrict__ sxT,
                                                             int ld, uint8_t* __restrict__ xq_out,
-                                                            float* __restrict__ sx_out) {
+                                                            float* __restrict__ sx_out, uint32_t* status) {
     __shared__ int dest[MAX_TOPK + 1];
     const int t = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_trigger();
     pdl_wait();
     const int nd = k + (n_shared ? 1 : 0);
-    if (threadIdx.x < k) dest[threadIdx.x] = inv_int[(size_t)t * k + threadIdx.x];
+    if (threadIdx.x < k) {
+        // a row outside the permuted buffers is flagged and skipped, never written
+        const int row = inv_int[(size_t)t * k + threadIdx.x];
+        const bool ok = row >= 0 && row < ld;
+        if (!ok && blockIdx.y == 0) atomicOr(status, MOE_DEV_BAD_ROW);
+        dest[threadIdx.x] = ok ? row : -1;
+    }
     if (threadIdx.x == 0 && n_shared) dest[k] = offsets_pad[E] + t;
     __syncthreads();
     const int G = H / QB;
@@ -606,6 +612,7 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __re
         const uint32_t q = pack4_e4m3(__fdiv_rn(v0, sc), __fdiv_rn(v1, sc), __fdiv_rn(v2, sc), __fdiv_rn(v3, sc));
         for (int d = 0; d < nd; ++d) {
             const int row = dest[d];
+            if (row < 0) continue;
             const int chunk = (lane >> 2) ^ (row & 7);
             *reinterpret_cast<uint32_t*>(xp + act_offset(g, row, ld) + chunk * 16 + (lane & 3) * 4) = q;
             if (lane == 0) sxT[(size_t)g * ld + row] = sc;
@@ -624,7 +631,8 @@ cudaError_t launch_quant_scatter(const moe_layer* L, const uint16_t* x, int T, c
                                            reinterpret_cast<const int32_t*>(ws + lay.inv_int),
                                            reinterpret_cast<const int32_t*>(ws + lay.offsets_pad), L->d.n_experts,
                                            reinterpret_cast<uint8_t*>(ws + lay.xp),
-                                           reinterpret_cast<float*>(ws + lay.sxT), lay.rows_pad, xq_out, sx_out);
+                                           reinterpret_cast<float*>(ws + lay.sxT), lay.rows_pad, xq_out, sx_out,
+                                           L->dev_status);
 }
 
 }  // namespace moe

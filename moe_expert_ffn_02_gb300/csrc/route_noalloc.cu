@@ -60,18 +60,15 @@ moe::WsLayout route_layout(const moe_layer* L, int T) {
     return l;
 }
 
-// Once per device, with that device current: the device address of the
-// array.  Runs on the first call of the entry point on each device.
+// Once per device: the device address of the array, looked up with that
+// device current (the caller has checked that `device` is the current one).
+// Runs on the first call of the entry point on each device.
 moe_status scratch_on(int device, void** out) {
     if (device < 0 || device >= kMaxDevices) return noalloc_fail(MOE_ERR_UNSUPPORTED, "device index out of range");
     std::lock_guard<std::mutex> lk(g_setup_mu);
     if (!g_scratch_addr[device]) {
-        int cur = -1;
-        cudaError_t e = cudaGetDevice(&cur);
-        if (e == cudaSuccess && cur != device) e = cudaSetDevice(device);
         void* p = nullptr;
-        if (e == cudaSuccess) e = cudaGetSymbolAddress(&p, g_route_scratch);
-        if (cur >= 0 && cur != device) cudaSetDevice(cur);
+        cudaError_t e = cudaGetSymbolAddress(&p, g_route_scratch);
         if (e != cudaSuccess || !p)
             return noalloc_fail(MOE_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
         g_scratch_addr[device] = p;
@@ -86,6 +83,12 @@ extern "C" __attribute__((visibility("default"))) moe_status moe_route_from_logi
     moe_layer* L, const float* logits, int32_t T, const moe_route_out* out, void* stream) {
     moe::set_last_error("");
     if (!L) return noalloc_fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+    int cur = -1;
+    cudaError_t ge = cudaGetDevice(&cur);
+    if (ge != cudaSuccess) return noalloc_fail(MOE_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(ge));
+    if (cur != L->device)
+        return noalloc_fail(MOE_ERR_INVALID_ARG, "the current device (" + std::to_string(cur) +
+                                                     ") is not the layer's device (" + std::to_string(L->device) + ")");
     if (T < 0) return noalloc_fail(MOE_ERR_INVALID_ARG, "T is negative");
     if (T > 0 && !logits) return noalloc_fail(MOE_ERR_INVALID_ARG, "logits is NULL");
     if (logits && (reinterpret_cast<uintptr_t>(logits) % 16))
@@ -116,7 +119,7 @@ extern "C" __attribute__((visibility("default"))) moe_status moe_route_from_logi
     if (e == cudaSuccess && out && out->topk_w)
         e = cudaMemcpyAsync(out->topk_w, w, sizeof(float) * (size_t)T * k, cudaMemcpyDeviceToDevice, s);
     if (e == cudaSuccess)
-        e = moe::launch_permute(L, ids, T, lay, ws, 64, out ? out->expert_offsets : nullptr,
+        e = moe::launch_permute(L, ids, T, lay, ws, moe::DEC_TILE_N, out ? out->expert_offsets : nullptr,
                                 out ? out->sorted_token : nullptr, out ? out->inv_row : nullptr, s);
     if (e != cudaSuccess) return noalloc_fail(MOE_ERR_CUDA, cudaGetErrorString(e));
     return MOE_OK;

@@ -88,7 +88,30 @@ def test_null_handle_calls_fail_cleanly(lib):
     assert lib.moe_forward_decode(None, None, 1, None, None, None, 0, None) == 1
     assert lib.moe_route(None, None, 0, None, None, 0, None) == 1
     assert lib.moe_destroy(None) == 1
+    assert lib.moe_debug_inject(None, 1) == 1
     assert moe.moe_status_string(3) == "MOE_ERR_WORKSPACE"
+
+
+def test_device_check_comes_before_any_other_use_of_the_handle(lib):
+    """Entries that enqueue work first compare the current device with the
+    one the layer was created on, and return before touching anything else.
+    The stand-in handle records device 7 and holds nothing else (its
+    pointers are NULL): without a GPU the device query itself fails
+    (MOE_ERR_CUDA), on a machine with fewer than 8 GPUs the devices differ
+    (MOE_ERR_INVALID_ARG); either way the call returns cleanly."""
+    import torch
+    fake = (ctypes.c_int32 * 4096)()
+    fake[6] = 7                                 # the device field follows the 24-byte descriptor
+    no_gpu = not torch.cuda.is_available()
+    for st in (lib.moe_forward_prefill(fake, 0x1000, 8, 0x1000, None, 0x1000, 1 << 30, None),
+               lib.moe_forward_decode(fake, 0x1000, 8, 0x1000, None, 0x1000, 1 << 30, None),
+               lib.moe_route_from_logits_noalloc(fake, 0x1000, 8, None, None),
+               lib.moe_tiles_load(fake, 0x1000, None)):
+        msg = moe.moe_last_error()
+        if no_gpu:
+            assert st == 4 and "cudaGetDevice" in msg, (st, msg)
+        else:
+            assert st == 1 and "is not the layer's device (7)" in msg, (st, msg)
 
 
 def test_plain_c_caller_compiles_links_and_gets_a_status(lib, tmp_path):

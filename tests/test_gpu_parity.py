@@ -204,6 +204,76 @@ def test_bounded_wait_reports_timeout_without_fault(h):
     layer.close()
 
 
+def _raw_forward(layer, x_bits, mode):
+    """One forward call without the status assertion of run_forward."""
+    import moe_expert_ffn_02_gb300 as moe
+    T = x_bits.shape[0]
+    x = torch.from_numpy(np.ascontiguousarray(x_bits).view(np.int16)).cuda()
+    y = torch.zeros_like(x)
+    ws, nb = layer.workspace(T, mode)
+    fn = moe.moe_forward_prefill if mode == moe.MODE_PREFILL else moe.moe_forward_decode
+    fn(layer.handle, x.data_ptr(), T, y.data_ptr(), None, ws, nb, layer.stream)
+    st, flags = moe.moe_get_device_status(layer.handle, layer.stream)
+    return st, flags, y.cpu().numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("mode,T", [(1, 200), (2, 16)])
+def test_planted_faults_are_flagged_without_a_fault(h, mode, T):
+    """Fault injection on the host side (moe_debug_inject): a routing id
+    outside [0, E) planted between top-k and grouping, and an internal row
+    outside the permuted buffers planted after grouping.  The kernels must
+    flag each in the device word (MOE_ERR_DEVICE_CHECK with the fault's bit),
+    clamp or skip it so nothing leaves the buffers, and the context must stay
+    usable: the next clean call gives the clean output bit for bit."""
+    import moe_expert_ffn_02_gb300 as moe
+    wl = small_wl(16, 4, H=384, I=256, T=T)
+    inp = synth.make_inputs(wl, seed=13)
+    layer = h.make_layer(wl, inp)
+    st, flags, y0 = _raw_forward(layer, inp["x"], mode)
+    assert (st, flags) == (0, 0)
+    for fault in (moe.DEV_BAD_EXPERT_ID, moe.DEV_BAD_ROW):
+        moe.moe_debug_inject(layer.handle, fault)
+        st, flags, _ = _raw_forward(layer, inp["x"], mode)
+        assert st == 5 and flags == fault, (fault, st, flags)      # MOE_ERR_DEVICE_CHECK, that bit only
+        st, flags, y1 = _raw_forward(layer, inp["x"], mode)          # fires once; the context is intact
+        assert (st, flags) == (0, 0)
+        assert np.array_equal(y1, y0)
+    with pytest.raises(moe.MoeError):
+        moe.moe_debug_inject(layer.handle, moe.DEV_WAIT_TIMEOUT)     # not a plantable fault
+    layer.close()
+
+
+def test_calls_on_another_device_are_rejected(h):
+    """A handle records the device it was created on; a call made while
+    another device is current is rejected before anything is enqueued.  With
+    one GPU the mismatch is shown with a stand-in handle that records device
+    7 (the handle's device field follows its 24-byte descriptor)."""
+    import ctypes
+    import moe_expert_ffn_02_gb300 as moe
+    lib = moe.load()
+    fake = (ctypes.c_int32 * 4096)()
+    fake[6] = 7
+    x = torch.zeros((8, 256), dtype=torch.int16, device="cuda")
+    y = torch.full_like(x, 5)
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    calls = [
+        lambda: lib.moe_forward_prefill(fake, x.data_ptr(), 8, y.data_ptr(), None, ws.data_ptr(), ws.numel(), None),
+        lambda: lib.moe_forward_decode(fake, x.data_ptr(), 8, y.data_ptr(), None, ws.data_ptr(), ws.numel(), None),
+        lambda: lib.moe_route(fake, x.data_ptr(), 8, None, ws.data_ptr(), ws.numel(), None),
+        lambda: lib.moe_route_from_logits(fake, ws.data_ptr(), 8, None, ws.data_ptr(), ws.numel(), None),
+        lambda: lib.moe_route_from_logits_noalloc(fake, ws.data_ptr(), 8, None, None),
+        lambda: lib.moe_forward_host(fake, 1, 0x1000, 8, 0x1000, ws.data_ptr(), ws.numel(), None),
+        lambda: lib.moe_tiles_load(fake, ws.data_ptr(), None),
+        lambda: lib.moe_debug_timeout_probe(fake, None),
+        lambda: lib.moe_profile_enable(fake, 1),
+    ]
+    for call in calls:
+        assert call() == 1                                   # MOE_ERR_INVALID_ARG
+        assert "is not the layer's device (7)" in moe.moe_last_error()
+    torch.cuda.synchronize()
+    assert bool((y == 5).all())
+
+
 def test_argument_errors_enqueue_nothing(h):
     import moe_expert_ffn_02_gb300 as moe
     wl = synth.WORKLOADS["tiny"]
@@ -227,16 +297,26 @@ def test_argument_errors_enqueue_nothing(h):
 
 # ------------------------------------------------------------------ full-size configurations
 
-def sample_rows(T, r, n_rand=48, seed=0):
-    """Tokens to check one by one: both ends, random ones, and every token of
-    the most loaded expert (up to 64) so a full multi-tile group is covered."""
+def group_edge_tokens(r):
+    """The first and the last token of every expert's group: the rows at the
+    boundaries of every group's first and last tile."""
+    off, st = r["offsets"], r["sorted_token"]
+    toks = set()
+    for e in range(len(off) - 1):
+        if off[e + 1] > off[e]:
+            toks.add(int(st[off[e]]))
+            toks.add(int(st[off[e + 1] - 1]))
+    return toks
+
+
+def sample_rows(T, r, n_rand, seed=0):
+    """Tokens to check one by one: both ends of the batch, a seeded random
+    subset of n_rand tokens, and the first and last token of every expert's
+    group."""
     rng = np.random.default_rng(seed)
     rows = set(range(min(8, T))) | set(range(max(0, T - 8), T))
     rows |= set(rng.choice(T, size=min(n_rand, T), replace=False).tolist())
-    counts = np.diff(r["offsets"])
-    hot = int(np.argmax(counts))
-    hot_tokens = r["sorted_token"][r["offsets"][hot]:r["offsets"][hot + 1]]
-    rows |= set(hot_tokens[:32].tolist()) | set(hot_tokens[-32:].tolist())
+    rows |= group_edge_tokens(r)
     return np.array(sorted(rows), dtype=np.int32)
 
 
@@ -265,41 +345,65 @@ def ds_inputs():
     return synth.make_inputs(wl, seed=0)
 
 
-@pytest.mark.parametrize("name", ["ds_prefill_8k", "skew_32k"])
-def test_deepseek_prefill_layers_sampled(h, ds_inputs, name):
-    wl = synth.WORKLOADS[name]
-    inp = dict(ds_inputs, x=synth.bf16_normal(0, synth.STREAM_X, (wl.T, wl.hidden)), router_b=synth.router_bias(wl, 0))
+def _prefill_full_size(h, wl, inp, n_rand):
+    """The full-size prefill layer through the C ABI, routing checked bit for
+    bit on every token, logits / quantised x / layer output on the tokens
+    `rows` (every token when n_rand is None).  Returns what the caller needs
+    for further checks."""
     layer = h.make_layer(wl, inp)
     y, dbg = h.run_forward(layer, inp["x"], 1)
     r = h.route(layer, inp["x"])
     ref_route = oracle.route_from_logits(r["logits"], wl.top_k)
     h.assert_routing_equal(dbg, ref_route)
-    counts = np.diff(ref_route["offsets"])
-    if name == "skew_32k":
-        mean = wl.T * wl.top_k / wl.n_experts
-        assert counts.max() > 10 * mean and counts.min() == 0
-    rows = sample_rows(wl.T, ref_route)
-    sub = np.sort(rows)
+    rows = None if n_rand is None else sample_rows(wl.T, ref_route, n_rand)
+    sub = np.arange(wl.T) if rows is None else rows
     Lref = oracle.logits(inp["x"][sub], inp["router_w"], inp["router_b"])
     assert np.all(np.abs(r["logits"][sub] - Lref) <= 1e-5 * (1 + np.abs(Lref)))
     h.count_routing_switches(r["topk_ids"][sub], Lref, wl.top_k)
     xq, sx = oracle.quant_1x128(synth.bf16_to_f32(inp["x"][sub]))
     assert np.array_equal(dbg["xq"][sub], xq) and np.array_equal(dbg["sx"][sub], sx)
-    h.check_layer_output(inp, wl.top_k, dbg, y, rows=sub)
+    h.check_layer_output(inp, wl.top_k, dbg, y, rows=rows)
+    return layer, dbg, ref_route
+
+
+def test_deepseek_prefill_8k_every_token(h, ds_inputs):
+    """The 8K-token DeepSeek-V3 prefill layer, every one of its 8,192 tokens
+    against the oracle (about 1.5 minutes of oracle time on 16 cores)."""
+    wl = synth.WORKLOADS["ds_prefill_8k"]
+    inp = dict(ds_inputs, x=synth.bf16_normal(0, synth.STREAM_X, (wl.T, wl.hidden)))
+    layer, _, _ = _prefill_full_size(h, wl, inp, None)
     layer.close()
 
 
-def test_kimi_prefill_layer_sampled(h):
+def _hottest(ref_route):
+    counts = np.diff(ref_route["offsets"])
+    return int(np.argmax(counts)), counts
+
+
+def test_skewed_32k_prefill_subset_and_hottest_expert(h, ds_inputs):
+    """The Zipf-skewed 32K layer: a seeded subset of 4,096 tokens plus the
+    first and last token of every group against the whole-layer oracle, and
+    every token routed to the hottest expert (about 32,000: every tile of
+    the largest group) against that expert alone."""
+    wl = synth.WORKLOADS["skew_32k"]
+    inp = dict(ds_inputs, x=synth.bf16_normal(0, synth.STREAM_X, (wl.T, wl.hidden)), router_b=synth.router_bias(wl, 0))
+    layer, dbg, ref_route = _prefill_full_size(h, wl, inp, 4096)
+    hot, counts = _hottest(ref_route)
+    mean = wl.T * wl.top_k / wl.n_experts
+    assert counts.max() > 10 * mean and counts.min() == 0
+    n = h.check_hot_expert(layer, inp, wl.top_k, dbg, inp["x"], 1, hot)
+    assert n == counts[hot]
+    layer.close()
+
+
+def test_kimi_prefill_layer_subset_and_hottest_expert(h):
+    """The Kimi-K2-shaped 64K layer (384 experts): a seeded subset of 4,096
+    tokens plus every group's first and last token against the whole-layer
+    oracle, and every token of the hottest expert against that expert."""
     wl = synth.WORKLOADS["kimi_64k"]
     inp = synth.make_inputs(wl, seed=0)
-    layer = h.make_layer(wl, inp)
-    y, dbg = h.run_forward(layer, inp["x"], 1, want_dbg=True)
-    r = h.route(layer, inp["x"])
-    ref_route = oracle.route_from_logits(r["logits"], wl.top_k)
-    h.assert_routing_equal(dbg, ref_route)
-    rows = sample_rows(wl.T, ref_route, n_rand=32)
-    Lref = oracle.logits(inp["x"][rows], inp["router_w"], inp["router_b"])
-    assert np.all(np.abs(r["logits"][rows] - Lref) <= 1e-5 * (1 + np.abs(Lref)))
-    h.count_routing_switches(r["topk_ids"][rows], Lref, wl.top_k)
-    h.check_layer_output(inp, wl.top_k, dbg, y, rows=rows)
+    layer, dbg, ref_route = _prefill_full_size(h, wl, inp, 4096)
+    hot, counts = _hottest(ref_route)
+    n = h.check_hot_expert(layer, inp, wl.top_k, dbg, inp["x"], 1, hot)
+    assert n == counts[hot]
     layer.close()

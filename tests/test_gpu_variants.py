@@ -13,7 +13,8 @@
   4.3, expert deferral); checked against the oracle's fp64 partial sums.
 - Host-tile layers (moe_create_ex with MOE_CREATE_HOST_TILES) run through the
   two-slot ring of StreamedStack (the hybrid-inference article's
-  Stream-Loading Prefill): must equal the same layers kept in HBM, bit for bit.
+  Stream-Loading Prefill): must equal the same layers kept in HBM, bit for
+  bit, and each layer must match the oracle on its own input.
 """
 import numpy as np
 import pytest
@@ -229,6 +230,24 @@ def test_streamed_stack_equals_resident(h, mode, T):
         assert np.array_equal(y.cpu().numpy(), y_ref.cpu().numpy())
     for ly in hosted:
         assert moe.moe_get_device_status(ly.handle, 0) == (0, 0)
+
+    # each host-tile layer alone (a one-layer ring) against the oracle on its own input, routed by the
+    # GPU's fp32 logits (moe_route works on host-tile layers); the chain of one-layer rings must give the
+    # three-layer ring's output bit for bit
+    x_l = x0
+    for ly, inp in zip(hosted, inps):
+        y_l = torch.empty_like(x_l)
+        moe.StreamedStack([ly], mode, x_l, y_l).run()
+        torch.cuda.synchronize()
+        xb = x_l.cpu().numpy().view(np.uint16)
+        r = h.route(ly, xb)
+        ref_route = oracle.route_from_logits(r["logits"], wl.top_k)
+        assert np.array_equal(r["topk_ids"], ref_route["ids"])
+        assert np.array_equal(r["topk_w"].view(np.uint32), ref_route["w"].view(np.uint32))
+        _, y64 = oracle.forward(dict(inp, x=xb), wl.top_k, ref_route["ids"], ref_route["w"], want_f64=True)
+        close(y_l.cpu().numpy().view(np.uint16), y64, f"streamed layer, mode {mode}")
+        x_l = y_l
+    assert np.array_equal(x_l.cpu().numpy(), y_ref.cpu().numpy())
 
     # a host-tile layer needs a slot; a resident layer has nothing to load
     ws1, nb1 = hosted[0].workspace(T, mode)

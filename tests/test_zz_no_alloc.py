@@ -4,8 +4,9 @@ against the workspace entry point, moe_route_from_logits, through the C ABI.
 The no-allocation variant is for callers that cannot allocate device memory
 when they route (serving runtimes that give all of HBM to their own pools at
 start-up, plain C callers without an allocator): its scratch is an array
-built into the library.  Both entry points run the same kernels, so their
-results must agree bit for bit.  This file is collected last so that a run
+built into the library.  Both entry points compute with the same device
+functions (for decode-sized batches the workspace entry fuses them into one
+kernel), so their results must agree bit for bit.  This file is collected last so that a run
 that stops at the first failure has already run every other test."""
 import numpy as np
 import pytest
@@ -24,21 +25,27 @@ def _routing_buffers(T, E, k):
     }
 
 
-def test_noalloc_routing_matches_workspace_routing_on_two_calls():
+@pytest.mark.parametrize("E,sizes", [(256, (1000, 3000)), (256, (1, 16, 64)), (640, (64, 200))])
+def test_noalloc_routing_matches_workspace_routing_on_two_calls(E, sizes):
+    """Calls in a row of different sizes.  Decode-sized batches (T <= 64 with
+    E <= 512) take the workspace entry's fused one-CTA routing kernel, while
+    this entry runs the stages one by one; E = 640 takes the multi-kernel
+    path on both sides."""
     import synth
     import moe_expert_ffn_02_gb300 as moe
     import _harness as h
 
     assert torch.cuda.is_available()
     moe.load()
-    wl = synth.Workload("route", 64, 128, 128, 256, 8)
+    wl = synth.Workload("route", 64, 128, 128, E, 8)
     layer = h.make_layer(wl, synth.make_inputs(wl, seed=4))
     E, k = wl.n_experts, wl.top_k
-    rng = np.random.default_rng(42)
-    for call, T in enumerate((1000, 3000)):             # two calls in a row, different sizes
+    rng = np.random.default_rng(42 + E + sizes[0])
+    for call, T in enumerate(sizes):                    # calls in a row, different sizes
         L = rng.normal(0, 1, (T, E)).astype(np.float32)
         L[0, :] = 0.5                                     # ties -> lowest indices
-        L[1] = np.round(L[1] * 2) / 2
+        if T > 1:
+            L[1] = np.round(L[1] * 2) / 2
         Ld = torch.from_numpy(L).cuda()
         ref = _routing_buffers(T, E, k)
         ws, nbytes = layer.workspace(T, moe.MODE_ROUTE)
@@ -54,6 +61,9 @@ def test_noalloc_routing_matches_workspace_routing_on_two_calls():
         st, flags = moe.moe_get_device_status(layer.handle, layer.stream)
         assert st == 0 and flags == 0
 
+    if E != 256 or sizes[0] != 1000:
+        layer.close()
+        return
     # beyond the built-in scratch: rejected before anything runs
     T = 40000
     Ld = torch.zeros((T, E), dtype=torch.float32, device="cuda")
