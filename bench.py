@@ -20,6 +20,12 @@ separate untimed steps.  e2e: the same layer through
 moe_forward_host from pinned host buffers (copies included).  cpu_baseline:
 the CPU oracle on the host cores, on a bounded sample of the workload.
 
+With a DeepSeek-V3 decode workload (the default), the same run also times
+the 8K-token DeepSeek-V3 prefill layer on the same weights and reports it
+under "prefill_8k" (tokens per second, the tensor-core roofline of the
+dominant expert GEMM, the whole-layer roofline, e2e and its own oracle
+baseline); --no-prefill-beside skips it.
+
 --impl reference times the CPU oracle itself (there is no other reference
 implementation of this layer) on the same workload and prints the same line
 with "impl": "reference".
@@ -62,6 +68,8 @@ def parse():
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-prefill-beside", action="store_true",
+                   help="decode workloads: skip the 8K-token prefill record timed in the same run")
     p.add_argument("--no-graph", action="store_true", help="decode: time plain launches instead of a graph replay")
     p.add_argument("--layers", type=int, default=1,
                    help="> 1: time a stack of this many layers (distinct weight copies in HBM, distinct routers), "
@@ -237,31 +245,19 @@ def run_reference(a, wl):
 
 # ---------------------------------------------------------------------------- our arm
 
-def run_ours(a, wl):
+def time_layer(a, layer, wl, x_np, steps, world, local):
+    """Warm-up, diagnostic and timed steps of one workload on `layer`; returns
+    the fields of a bench line (value, roofline of the dominant kernel, whole
+    layer roofline, end-to-end figure, clocks, stage split)."""
     import torch
     import torch.distributed as dist
 
     import moe_expert_ffn_02_gb300 as moe
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    moe.load()
     metric, unit, hib = metric_of(wl)
-    inp = synth.make_inputs(wl, seed=a.seed)
-    dev = {k: (torch.from_numpy(np.ascontiguousarray(v)).cuda() if v is not None else None)
-           for k, v in inp.items() if k != "x"}
-    layer = moe.Layer(wl.hidden, wl.inter, wl.n_experts, wl.top_k, dev, n_shared=wl.n_shared)
-    del dev
-    torch.cuda.empty_cache()
     T, H = wl.T, wl.hidden
     mode = moe.MODE_DECODE if is_decode(wl) else moe.MODE_PREFILL
     stream = torch.cuda.current_stream()
-    x = torch.from_numpy(inp["x"].view(np.int16)).cuda()
+    x = torch.from_numpy(x_np.view(np.int16)).cuda()
     y = torch.empty_like(x)
     ws, nbytes = layer.workspace(T, mode)
     fwd = moe.moe_forward_decode if mode == moe.MODE_DECODE else moe.moe_forward_prefill
@@ -311,15 +307,15 @@ def run_ours(a, wl):
             flush.zero_()
             graph.replay()
         torch.cuda.synchronize()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     stage_ms = []
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         t_wall = time.perf_counter()
-        for i in range(a.steps):
+        for i in range(steps):
             flush.zero_()
             starts[i].record(stream)
             graph.replay() if graph is not None else step()
@@ -328,6 +324,7 @@ def run_ours(a, wl):
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
     moe.moe_profile_enable(layer.handle, False)
+    del graph
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_s = sum(step_ms) / 1e3
     if world > 1:
@@ -335,11 +332,11 @@ def run_ours(a, wl):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_s = float(t.item())
         dist.barrier()
-    sec_per_step = total_s / a.steps
+    sec_per_step = total_s / steps
     value = value_of(wl, sec_per_step, world)
     # kernels per step: decode-sized batches (T <= 64) route in 2 (logits GEMV, one-CTA top-k and grouping),
     # larger ones in 5 (logits GEMM, top-k, count, scan, scatter); then quantise, gate/up, down, combine
-    n_launches = (6 if T <= 64 else 9) * a.steps
+    n_launches = (6 if T <= 64 else 9) * steps
 
     # ---------------------------------------------- roofline of the dominant kernel
     pk = peaks()
@@ -382,13 +379,13 @@ def run_ours(a, wl):
     # ---------------------------------------------- end to end through the host entry
     e2e = None
     if not a.no_e2e:
-        xh = torch.from_numpy(inp["x"].view(np.int16)).pin_memory()
+        xh = torch.from_numpy(x_np.view(np.int16)).pin_memory()
         yh = torch.empty_like(xh).pin_memory()
         ws_h, nb_h = layer.workspace(T, mode)
         for _ in range(2):
             moe.moe_forward_host(layer.handle, mode, xh.data_ptr(), T, yh.data_ptr(), ws_h, nb_h, stream.cuda_stream)
         e_ms = []
-        for _ in range(a.steps):
+        for _ in range(steps):
             flush.zero_()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
@@ -398,35 +395,91 @@ def run_ours(a, wl):
             e_ms.append(e0.elapsed_time(e1))
         e2e = {"value": value_of(wl, statistics.mean(e_ms) / 1e3, world), "unit": unit,
                "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2}
+    del x, y, flush
+    torch.cuda.empty_cache()
+    return {
+        "metric": metric, "value": value, "unit": unit, "steps": steps, "ms_per_step": sec_per_step * 1e3,
+        "higher_is_better": hib, "roofline": roof, "layer_roofline": layer_roof, "e2e": e2e,
+        "gpu_launches": n_launches * world, "clocks": clk.summary(), "stage_ms": mean_stage,
+        "touched_experts": n_touched, "wall_s_timed_region": t_wall, "tokens_per_s": T * world / sec_per_step,
+        "graph": use_graph,
+    }
 
-    # ---------------------------------------------- CPU oracle baseline (rank 0, N = 1)
+
+def cpu_baseline_of(wl, inp_x, router_inp, target_s):
+    """The oracle on the host cores on the first tokens of the workload, scaled to its unit."""
+    import oracle
+    oracle.build()
+    n_tok = oracle_sample_plan(wl, target_s=target_s)
+    sec = time_oracle(wl, dict(router_inp, x=inp_x), np.arange(n_tok))
+    return {"value": cpu_value(wl, sec, n_tok), "unit": metric_of(wl)[1], "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"first {n_tok} of {wl.T} tokens (logits, routing, experts, combine), scaled to the workload"}
+
+
+def config_of(wl, world, graph):
+    return {"workload": wl.name, "T": wl.T, "hidden": wl.hidden, "inter": wl.inter, "n_experts": wl.n_experts,
+            "top_k": wl.top_k, "n_shared": wl.n_shared, "parallelism": f"replicas{world}", "graph": graph,
+            "l2": "flushed between steps (512 MiB write, outside the timed events)"}
+
+
+# The prefill workload timed beside a decode workload of the same layer
+# shapes (DeepSeek-V3: the decode layers' weights are the 8K prefill layer's).
+PREFILL_BESIDE = {"ds_decode_t1": "ds_prefill_8k", "ds_decode_t4": "ds_prefill_8k", "ds_decode_t16": "ds_prefill_8k"}
+
+
+def run_ours(a, wl):
+    import torch
+    import torch.distributed as dist
+
+    import moe_expert_ffn_02_gb300 as moe
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    moe.load()
+    inp = synth.make_inputs(wl, seed=a.seed)
+    dev = {k: (torch.from_numpy(np.ascontiguousarray(v)).cuda() if v is not None else None)
+           for k, v in inp.items() if k != "x"}
+    layer = moe.Layer(wl.hidden, wl.inter, wl.n_experts, wl.top_k, dev, n_shared=wl.n_shared)
+    del dev
+    torch.cuda.empty_cache()
+    rec = time_layer(a, layer, wl, inp["x"], a.steps, world, local)
+
+    # the 8K-token prefill layer on the same weights, timed in the same run
+    sub = None
+    pname = None if a.no_prefill_beside else PREFILL_BESIDE.get(wl.name)
+    if pname:
+        pw = synth.WORKLOADS[pname]
+        px = synth.bf16_normal(a.seed, synth.STREAM_X, (pw.T, pw.hidden))
+        sub = time_layer(a, layer, pw, px, min(a.steps, 20), world, local)
+        sub["config"] = config_of(pw, world, sub.pop("graph"))
+        sub["dtype"] = "fp8_e4m3"
+        if not a.no_cpu_baseline and rank == 0 and world == 1:
+            sub["cpu_baseline"] = cpu_baseline_of(pw, px, inp, 8.0)
+
     cpu = None
     if not a.no_cpu_baseline and rank == 0 and world == 1:
-        import oracle
-        oracle.build()
-        n_tok = oracle_sample_plan(wl, target_s=12.0)
-        rows_s = np.arange(n_tok)
-        sec = time_oracle(wl, inp, rows_s)
-        cpu = {"value": cpu_value(wl, sec, n_tok), "unit": unit, "cores": oracle.threads(), "kind": "oracle",
-               "sample": f"first {n_tok} of {T} tokens (logits, routing, experts, combine), scaled to the workload"}
+        cpu = cpu_baseline_of(wl, inp["x"], inp, 12.0)
 
     layer.close()
     if rank == 0:
         line = {
-            "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
-            "ms_per_step": sec_per_step * 1e3, "higher_is_better": hib, "scaling": "weak", "vs_baseline": None,
-            "dtype": "fp8_e4m3", "data": "synthetic",
-            "config": {"workload": wl.name, "T": T, "hidden": H, "inter": wl.inter, "n_experts": wl.n_experts,
-                       "top_k": wl.top_k, "n_shared": wl.n_shared, "parallelism": f"replicas{world}",
-                       "graph": graph is not None,
-                       "l2": "flushed between steps (512 MiB write, outside the timed events)"},
-            "roofline": roof, "layer_roofline": layer_roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": n_launches * world,
-            "clocks": clk.summary(), "stage_ms": mean_stage,
+            "metric": rec["metric"], "value": rec["value"], "unit": rec["unit"], "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": rec["ms_per_step"], "higher_is_better": rec["higher_is_better"],
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3", "data": "synthetic",
+            "config": config_of(wl, world, rec["graph"]),
+            "roofline": rec["roofline"], "layer_roofline": rec["layer_roofline"], "cpu_baseline": cpu,
+            "e2e": rec["e2e"], "gpu_launches": rec["gpu_launches"] + (sub["gpu_launches"] if sub else 0),
+            "clocks": rec["clocks"], "stage_ms": rec["stage_ms"],
             "stage_ms_note": "every stage timed in separate untimed steps; the timed steps carry only the "
-                             "dominant kernel's events", "touched_experts": n_touched,
-            "wall_s_timed_region": t_wall, "tokens_per_s": T * world / sec_per_step,
+                             "dominant kernel's events", "touched_experts": rec["touched_experts"],
+            "wall_s_timed_region": rec["wall_s_timed_region"], "tokens_per_s": rec["tokens_per_s"],
         }
+        if sub is not None:
+            line["prefill_8k"] = sub
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
