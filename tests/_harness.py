@@ -211,9 +211,11 @@ def check_layer_output(inp: dict, k: int, dbg: dict, y_gpu: np.ndarray, rows=Non
     routing by the caller).
 
     1) Against the oracle with its own h: rel-L2 <= 5e-3 against its bf16
-       y, and max-abs <= 3e-2 * rms against its unrounded fp64 y (the bf16
-       rounding of y then costs at most half a bf16 step, and a
-       boundary-flipped h code moves y by far less than that).
+       y; on the tokens whose h codes all equal the GPU's, max-abs <=
+       3e-2 * rms against its unrounded fp64 y (the bf16 rounding of y costs
+       at most half a bf16 step).  The max-abs over all tokens is printed:
+       one boundary-flipped code of a large h moves its token's y by up to
+       a few 1e-2 * rms, so that figure is not bounded by 3e-2.
     2) Its h codes against the GPU's: equal except at rounding boundaries
        (check_h_codes).
     3) Against the oracle evaluated with the GPU's h codes (the other valid
@@ -228,14 +230,18 @@ def check_layer_output(inp: dict, k: int, dbg: dict, y_gpu: np.ndarray, rows=Non
     b = synth.bf16_to_f32(y_ref).astype(np.float64)
     rms = np.sqrt(np.mean(y64 * y64))
     rel_plain = np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30)
-    mx_plain = np.max(np.abs(a - y64)) / max(rms, 1e-30) if a.size else 0.0
+    err = np.abs(a - y64).max(axis=1) / max(rms, 1e-30) if a.size else np.zeros(sel.size)
     flips = check_h_codes(dbg["hq"][sel], dbg["sh"][sel], href)
-    print(f"[parity] own-h rel_l2={rel_plain:.3e} max_abs(vs fp64)/rms={mx_plain:.3e} h boundary flips={flips} "
-          f"tokens={sel.size}")
-    assert rel_plain <= REL_L2_TOL, f"relative L2 error {rel_plain:.3e} > {REL_L2_TOL} (oracle's own h)"
-    assert mx_plain <= MAX_ABS_TOL, f"max abs error {mx_plain:.3e} * rms > {MAX_ABS_TOL} (oracle's own h, fp64 y)"
-    y_ov = y_ref.copy()
     changed = np.nonzero((dbg["hq"][sel] != href["hq"]).reshape(sel.size, -1).any(axis=1))[0]
+    same = np.ones(sel.size, bool)
+    same[changed] = False
+    mx_same = float(err[same].max()) if same.any() else 0.0
+    print(f"[parity] own-h rel_l2={rel_plain:.3e} max_abs(vs fp64)/rms={float(err.max()) if err.size else 0:.3e} "
+          f"(tokens without h flips: {mx_same:.3e}) h boundary flips={flips} tokens={sel.size} "
+          f"tokens with a flip={changed.size}")
+    assert rel_plain <= REL_L2_TOL, f"relative L2 error {rel_plain:.3e} > {REL_L2_TOL} (oracle's own h)"
+    assert mx_same <= MAX_ABS_TOL, f"max abs error {mx_same:.3e} * rms > {MAX_ABS_TOL} (oracle's own h, fp64 y)"
+    y_ov = y_ref.copy()
     if changed.size:
         y_ov[changed] = oracle.forward(inp, k, ids, w, rows=sel[changed], hq_in=dbg["hq"], sh_in=dbg["sh"])
     return compare_y(y_gpu[sel], y_ov)
@@ -253,7 +259,16 @@ def check_hot_expert(layer, inp: dict, k: int, dbg: dict, x_bits: np.ndarray, mo
     layer runs with the slot of `expert` deferred (moe_forward_deferred, same
     GEMMs, split combine), so y_next[t] = bf16(w O_expert(t)); the oracle
     evaluates only that expert for each such token (k = 1, no shared
-    expert), with its own h and with the GPU's h codes of that slot."""
+    expert).  Against the oracle's own h: rel-L2 <= 5e-3.  Against the
+    oracle's unrounded fp64 value under the GPU's h codes (its own h where
+    the codes agree): every element within half a bf16 step of it plus
+    3e-3 * rms -- the bf16 rounding of the output plus the error of the
+    tensor core's FP8 partial sums, which is absolute (of the order of the
+    summed terms, not of a result that cancels to near zero).  (The
+    layer's 3e-2 * rms max-abs bound alone is not the right scale here: one
+    expert's weighted output has heavier tails than the layer output, and
+    a rounding tie decided the other way at an element of many times the
+    rms is a full bf16 step.)"""
     T, H = x_bits.shape
     ids, w = dbg["topk_ids"], dbg["topk_w"]
     mask = (ids == expert).astype(np.uint8)
@@ -278,22 +293,28 @@ def check_hot_expert(layer, inp: dict, k: int, dbg: dict, x_bits: np.ndarray, mo
     y_ref, y64, href = oracle.forward(one, 1, ids1, w1, rows=toks, want_f64=True, want_h=True)
     a = synth.bf16_to_f32(y_gpu).astype(np.float64)
     b = synth.bf16_to_f32(y_ref).astype(np.float64)
-    rms = np.sqrt(np.mean(y64 * y64))
     rel_plain = np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30)
-    mx_plain = np.max(np.abs(a - y64)) / max(rms, 1e-30)
     ghq = dbg["hq"][toks, slot][:, None, :]
     gsh = dbg["sh"][toks, slot][:, None, :]
     flips = check_h_codes(ghq, gsh, href)
-    print(f"[hot expert {expert}] tokens={toks.size} own-h rel_l2={rel_plain:.3e} "
-          f"max_abs(vs fp64)/rms={mx_plain:.3e} h flips={flips}")
-    assert rel_plain <= REL_L2_TOL and mx_plain <= MAX_ABS_TOL
-    y_ov = y_ref.copy()
     changed = np.nonzero((ghq != href["hq"]).reshape(toks.size, -1).any(axis=1))[0]
+    y64_ov = y64.copy()
     if changed.size:
         hq_full = np.zeros((T, 1, ghq.shape[-1]), np.uint8)
         sh_full = np.ones((T, 1, gsh.shape[-1]), np.float32)
         hq_full[toks] = ghq
         sh_full[toks] = gsh
-        y_ov[changed] = oracle.forward(one, 1, ids1, w1, rows=toks[changed], hq_in=hq_full, sh_in=sh_full)
-    compare_y(y_gpu, y_ov)
+        _, y64_ov[changed] = oracle.forward(one, 1, ids1, w1, rows=toks[changed], hq_in=hq_full, sh_in=sh_full,
+                                            want_f64=True)
+    rms = np.sqrt(np.mean(y64_ov * y64_ov))
+    mag = np.abs(y64_ov)
+    half_step = np.ldexp(1.0, np.floor(np.log2(np.maximum(mag, 1e-300))).astype(np.int64) - 8)
+    err = np.abs(a - y64_ov)
+    worst = float(np.max(err / (half_step + 3e-3 * rms)))
+    rel_ov = np.linalg.norm(a - y64_ov) / max(np.linalg.norm(y64_ov), 1e-30)
+    print(f"[hot expert {expert}] tokens={toks.size} own-h rel_l2={rel_plain:.3e} h flips={flips} "
+          f"vs fp64 (GPU h): rel_l2={rel_ov:.3e} max_abs/rms={float(err.max()) / rms:.3e} "
+          f"max err / (half bf16 step + 3e-3 rms)={worst:.3f}")
+    assert rel_plain <= REL_L2_TOL and rel_ov <= REL_L2_TOL
+    assert worst <= 1.0, "an element is further than half a bf16 step from the oracle's fp64 value"
     return toks.size
