@@ -17,13 +17,14 @@
 // article, Fig. 9-10: a 128-element block's partial sum is scaled once):
 // each TMEM lane is one token, so its activation scale s_x[token][kb] is a
 // per-thread scalar and the weight scales s_w[kb] are uniform; the epilogue
-// warps read each block's partial with tcgen05.ld and promote it with fp32
-// FMAs into registers (scalar FFMA on the loaded registers: packing them into
-// pairs for fma.rn.f32x2 costs more moves than it saves).  Both scales are
-// copied with the stage's operands into a scale ring of their own, so the
-// epilogue reads them from shared memory; a stage is free again once the
-// MMAs that read it have completed, a scale slot once every epilogue warp
-// has taken its scales.  Gate/up then forms h = SiLU(g)*u and its
+// warps read each block's partial with tcgen05.ld, 16 columns at a time,
+// and promote it into registers with packed fp32 FMAs (fma.rn.f32x2: two
+// lanes of the same IEEE fma per instruction, half the issue slots of scalar
+// FFMA).  Both scales are copied with the stage's operands into the stage's
+// scale slot; the epilogue warps read them once the block's MMAs have
+// completed and then hand the stage back themselves, so one commit per block
+// (on the TMEM buffer) serves both the epilogue and the producer.  Gate/up
+// then forms h = SiLU(g)*u and its
 // 1x128 E4M3 codes (the activation and elementwise product between gate/up
 // and down, "CPU fine-grained parallelism" section of the same article);
 // down writes fp32 output rows.
@@ -52,16 +53,15 @@ constexpr int STAGES = 4;
 constexpr int W_BYTES = 2 * TILE_BYTES;   // 256 weight rows
 constexpr int X_BYTES = BM * 128;         // 128 token rows
 constexpr int STAGE = W_BYTES + X_BYTES;
-// Scale ring: per k block the 128 tokens' activation scales (512 B) and the
-// weight-scale record (16 B), in SSLOTS slots of their own.  They are copied
-// with the stage (counted on its full barrier), but a stage is free as soon
-// as its MMAs complete, while a scale slot is freed by the epilogue warps
-// once they have read it.
+// Scale slot of each stage: the k block's 128 token activation scales
+// (512 B) and the weight-scale record (16 B), copied with the stage's
+// operands (counted on its full barrier).  The stage, slot included, is
+// handed back by the epilogue warps (EPI_WARPS arrivals on its empty
+// barrier) once they have read the scales, which is after the block's MMAs
+// completed.
 constexpr int S_BYTES = BM * 4;
 constexpr int R_BYTES = 16;
-constexpr int SSLOTS = 8;
 constexpr int SSLOT = S_BYTES + R_BYTES;
-static_assert(SSLOTS >= STAGES + 2, "a scale slot must outlive its stage and both TMEM buffers");
 // + amax exchange + the group table copy (units are decoded from shared
 // memory; up to 385 groups, larger tables are read in place) + the down
 // epilogue's per-warp staging tiles (32 rows x 16 floats, rows 20 floats
@@ -69,7 +69,7 @@ static_assert(SSLOTS >= STAGES + 2, "a scale slot must outlive its stage and bot
 constexpr int GT_SMEM_CAP = 386;
 constexpr int STG_STRIDE = 20;
 constexpr int STG_BYTES = EPI_WARPS * 32 * STG_STRIDE * 4;
-constexpr int SMEM = STAGES * STAGE + SSLOTS * SSLOT + 2 * 4 * 32 * 4 + gt_smem_bytes(GT_SMEM_CAP) + STG_BYTES + 256;
+constexpr int SMEM = STAGES * STAGE + STAGES * SSLOT + 2 * 4 * 32 * 4 + gt_smem_bytes(GT_SMEM_CAP) + STG_BYTES + 256;
 // dynamic (with 1024 bytes of alignment slack) + static (barriers, padded to 1024) <= 227 KB
 static_assert(SMEM + 1024 + 1024 <= 232448, "shared memory budget");
 
@@ -116,12 +116,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
-    uint8_t* sring = smem + STAGES * STAGE;                                 // [SSLOTS][SSLOT]
-    uint8_t* after = sring + SSLOTS * SSLOT;
+    uint8_t* sring = smem + STAGES * STAGE;                                 // [STAGES][SSLOT]
+    uint8_t* after = sring + STAGES * SSLOT;
     float* amax_x = reinterpret_cast<float*>(after);                       // [2 halves][4 quarters][32 lanes]
     int* gt_s = reinterpret_cast<int*>(after + 2 * 4 * 32 * 4);
     float* stg_all = reinterpret_cast<float*>(after + 2 * 4 * 32 * 4 + gt_smem_bytes(GT_SMEM_CAP));
-    __shared__ uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], sempty[SSLOTS];
+    __shared__ uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -135,8 +135,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
     const SGroups sg = load_groups(gt, gt_s, threadIdx.x, NTHREADS, GT_SMEM_CAP);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-        for (int s = 0; s < SSLOTS; ++s) mbar_init(&sempty[s], EPI_WARPS);
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], EPI_WARPS); }
         for (int b = 0; b < 2; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], EPI_WARPS); }
         fence_mbar_init();
         abort_flag = 0;
@@ -152,8 +151,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CTRL_REGS));
         if (warp == 0 && lane == 0) {
             // -------------------------------------------------------- producer
-            int stage = 0, slot = 0;
-            uint32_t phase = 0, sphase = 0, armed = 0, armed_par = 0;
+            int stage = 0;
+            uint32_t phase = 0, armed = 0, armed_par = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
                 const Unit un = decode_unit(sg, u, NB);
@@ -164,13 +163,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
                 const uint32_t wbytes = two ? (uint32_t)W_BYTES : (uint32_t)TILE_BYTES;
                 const uint8_t* wbase = a.w + ((size_t)(un.expert * MT128 + t0) * KT) * (GU ? W_BYTES : TILE_BYTES);
                 for (int kb = 0; kb < KT; ++kb) {
-                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, a.wait_limit, a.status, abort) ||
-                        !mbar_wait_bounded(&sempty[slot], sphase ^ 1u, a.wait_limit, a.status, abort)) {
+                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, a.wait_limit, a.status, abort)) {
                         ok = false;
                         break;
                     }
                     uint8_t* st = stages + stage * STAGE;
-                    uint8_t* ss = sring + slot * SSLOT;
+                    uint8_t* ss = sring + stage * SSLOT;
                     mbar_arrive_expect_tx(&full[stage], wbytes + X_BYTES + S_BYTES + R_BYTES);
                     if (GU) {
                         bulk_g2s(st, wbase + (size_t)kb * W_BYTES, W_BYTES, &full[stage]);
@@ -186,7 +184,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
                     armed |= 1u << stage;
                     armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-                    if (++slot == SSLOTS) { slot = 0; sphase ^= 1u; }
                 }
             }
             for (int s = 0; s < STAGES; ++s)
@@ -202,8 +199,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
                 const bool two = GU || (2 * wb + 1 < MT128);
                 const uint32_t idesc = idesc_for(two ? BN : BN / 2);
                 for (int kb = 0; kb < KT; ++kb) {
-                    if (!mbar_wait_bounded(&tempty[buf], tphase ^ 1u, a.wait_limit, a.status, abort) ||
-                        !mbar_wait_bounded(&full[stage], phase, a.wait_limit, a.status, abort)) {
+                    // the stage's copies usually land long before the buffer is handed back:
+                    // waiting for them first keeps that wait off the hand-off path
+                    if (!mbar_wait_bounded(&full[stage], phase, a.wait_limit, a.status, abort) ||
+                        !mbar_wait_bounded(&tempty[buf], tphase ^ 1u, a.wait_limit, a.status, abort)) {
                         ok = false;
                         break;
                     }
@@ -215,8 +214,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
                     mma_f8(dt, adesc + 2, bdesc + 2, idesc, 1u);
                     mma_f8(dt, adesc + 4, bdesc + 4, idesc, 1u);
                     mma_f8(dt, adesc + 6, bdesc + 6, idesc, 1u);
-                    mma_commit(&empty[stage]);
-                    mma_commit(&tfull[buf]);
+                    mma_commit(&tfull[buf]);          // the epilogue hands the stage back after this
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                     if (++buf == 2) { buf = 0; tphase ^= 1u; }
                 }
@@ -230,7 +228,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
         const int quarter = warp & 3;               // TMEM lanes this warp may read
         const int half = ew >> 2;                   // column half of the 256-column buffer
         const int r = quarter * 32 + lane;          // token row inside the tile
-        int buf = 0, slot = 0;
+        int buf = 0, slot = 0;                        // slot: the stage of the block (scales, empty barrier)
         uint32_t tphase = 0;
         bool dead = false;
         for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
@@ -242,43 +240,43 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
 #pragma unroll
             for (int c = 0; c < HALF; ++c) acc[c] = 0.f;
             for (int kb = 0; kb < KT; ++kb) {
-                // No wait on full[stage] here: the MMA thread waited for the stage's copies
-                // (scales included) to land before issuing the MMAs whose completion
-                // signals tfull, so they have landed by the time tfull completes.
                 if (!dead && !mbar_wait_bounded(&tfull[buf], tphase, a.wait_limit, a.status, abort)) dead = true;
                 if (!dead) {
                     tc_fence_after();
-                    // this block's scales from its scale slot: s_x of my token, the record's weight scales
+                    // this block's scales from its stage's slot: s_x of my token, the record's weight
+                    // scales; combined per 32-column chunk (gate/up: c0 gate, c1 up; down: my half's tile)
                     const uint8_t* tail = sring + slot * SSLOT;
                     const float sx = reinterpret_cast<const float*>(tail)[r];
                     const float2 sw = *reinterpret_cast<const float2*>(tail + S_BYTES);
+                    const float c0 = (GU || half == 0) ? sw.x * sx : sw.y * sx;
+                    const float c1 = sw.y * sx;
                     const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN);
-                    // Four 32-column chunks, software-pipelined: the next chunk's tcgen05.ld is
-                    // in flight while this chunk's FMAs issue, and the wait that follows them
-                    // covers that load.  Gate/up chunk i: gate (i even) or up (i odd) columns
-                    // [64h + 32(i/2), +32) of its 128-column tile, accumulators
-                    // 32(i%2) + 16(i/2); down: columns [128h + 32i, +32), accumulators 16i.
+                    // Eight 16-column pieces, software-pipelined: the next piece's tcgen05.ld is in
+                    // flight while this piece's FMAs issue.  32-column chunk i = piece / 2 covers, for
+                    // gate/up, gate (i even) or up (i odd) columns [64h + 32(i/2), +32) of its
+                    // 128-column tile into accumulators 64(i%2) + 32(i/2); for down, columns
+                    // [128h + 32i, +32) into accumulators 32i.
                     auto col_of = [&](int i) -> uint32_t {
                         return GU ? (uint32_t)((i & 1) * 128 + 64 * half + 32 * (i >> 1)) : (uint32_t)(128 * half + 32 * i);
                     };
-                    uint32_t pa[32], pb[32];
-                    tmem_ld32u(tb + col_of(0), pa);
-                    // combined scales s_w * s_x (gate/up: c0 gate, c1 up; down: my half's tile)
-                    const float c0 = (GU || half == 0) ? sw.x * sx : sw.y * sx;
-                    const float c1 = sw.y * sx;
+                    uint32_t pa[16], pb[16];
+                    tmem_ld16u(tb + col_of(0), pa);
+                    // the scales are in registers and the block's MMAs are complete: the stage,
+                    // scale slot included, can be refilled
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&sempty[slot]);
+                    if (lane == 0) mbar_arrive(&empty[slot]);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint32_t(&cur)[32] = (i & 1) ? pb : pa;
-                        uint32_t(&nxt)[32] = (i & 1) ? pa : pb;
-                        if (i < 3) tmem_ld32u(tb + col_of(i + 1), nxt);
+                    for (int j = 0; j < 8; ++j) {
+                        uint32_t(&cur)[16] = (j & 1) ? pb : pa;
+                        uint32_t(&nxt)[16] = (j & 1) ? pa : pb;
+                        if (j < 7) tmem_ld16u(tb + col_of((j + 1) >> 1) + 16 * ((j + 1) & 1), nxt);
+                        const int i = j >> 1;
                         const float c = (GU && (i & 1)) ? c1 : c0;
-                        const int base = GU ? ((i & 1) * 32 + (i >> 1) * 16) : 16 * i;
+                        const int base = 2 * (GU ? ((i & 1) * 32 + (i >> 1) * 16) : 16 * i) + 16 * (j & 1);
 #pragma unroll
-                        for (int q = 0; q < 32; ++q) acc[2 * base + q] = fmaf(__uint_as_float(cur[q]), c, acc[2 * base + q]);
-                        if (i < 3) tmem_wait_ld();
+                        for (int q = 0; q < 16; q += 2) fma2(acc[base + q], acc[base + q + 1], cur[q], cur[q + 1], c);
+                        if (j < 7) tmem_wait_ld();
                     }
                     tc_fence_before();
                     __syncwarp();
@@ -286,12 +284,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
                 } else {
                     __syncwarp();
                     if (lane == 0) {
-                        mbar_arrive(&sempty[slot]);
+                        mbar_arrive(&empty[slot]);
                         mbar_arrive(&tempty[buf]);
                     }
                 }
                 if (++buf == 2) { buf = 0; tphase ^= 1u; }
-                if (++slot == SSLOTS) slot = 0;
+                if (++slot == STAGES) slot = 0;
             }
 
             if (GU) {

@@ -60,7 +60,26 @@ __device__ __forceinline__ void tmem_ld32u(uint32_t taddr, uint32_t (&r)[32]) {
         : "memory");
 }
 
+// 32 lanes x 16 columns.
+__device__ __forceinline__ void tmem_ld16u(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// (a0, a1) = (x0 * c + a0, x1 * c + a1): two IEEE round-to-nearest fp32 fmas in
+// one packed instruction (x0, x1 raw fp32 bits as tcgen05.ld returns them).
+__device__ __forceinline__ void fma2(float& a0, float& a1, uint32_t x0, uint32_t x1, float c) {
+    asm("{\n .reg .b64 a, x, cc;\n mov.b64 a, {%0, %1};\n mov.b64 x, {%2, %3};\n mov.b64 cc, {%4, %4};\n"
+        " fma.rn.f32x2 a, x, cc, a;\n mov.b64 {%0, %1}, a;\n}"
+        : "+f"(a0), "+f"(a1)
+        : "r"(x0), "r"(x1), "f"(c));
+}
 
 // kind::f16 MMA (bf16 or f16 operands, same type for A and B), fp32 accumulate.
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
