@@ -222,7 +222,9 @@ def run_reference(a, wl):
     oracle.build()
     metric, unit, hib = metric_of(wl)
     inp = synth.make_inputs(wl, seed=a.seed)
-    n_tok = min(wl.T, max(1, oracle_sample_plan(wl, target_s=60.0 / max(1, a.steps + a.warmup))))
+    # at least one token per oracle thread: the oracle runs tokens in parallel, so a sample
+    # smaller than its thread count takes as long as a full one and would scale up wrongly
+    n_tok = min(wl.T, max(oracle.threads(), oracle_sample_plan(wl, target_s=60.0 / max(1, a.steps + a.warmup))))
     rows = np.arange(n_tok)
     for _ in range(a.warmup):
         time_oracle(wl, inp, rows[: max(1, n_tok // 4)])
@@ -410,7 +412,7 @@ def cpu_baseline_of(wl, inp_x, router_inp, target_s):
     """The oracle on the host cores on the first tokens of the workload, scaled to its unit."""
     import oracle
     oracle.build()
-    n_tok = oracle_sample_plan(wl, target_s=target_s)
+    n_tok = min(wl.T, max(oracle.threads(), oracle_sample_plan(wl, target_s=target_s)))
     sec = time_oracle(wl, dict(router_inp, x=inp_x), np.arange(n_tok))
     return {"value": cpu_value(wl, sec, n_tok), "unit": metric_of(wl)[1], "cores": oracle.threads(), "kind": "oracle",
             "sample": f"first {n_tok} of {wl.T} tokens (logits, routing, experts, combine), scaled to the workload"}
@@ -484,6 +486,24 @@ def run_ours(a, wl):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def host_copy_peak_gbps(nbytes: int = 2 << 30, reps: int = 3) -> float:
+    """The machine's host -> device copy rate: one copy from pinned host memory,
+    best of `reps` (the reference for the host-tile ring's streaming rate)."""
+    import torch
+    src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    best = 0.0
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dst.copy_(src, non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        best = max(best, nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    del src, dst
+    return best
 
 
 def run_layers(a, wl):
@@ -581,8 +601,11 @@ def run_layers(a, wl):
     if a.host_tiles:
         line["config"]["graph"] = False
         line["config"]["weights"] = "expert tiles in pinned host memory, streamed host->device per layer"
-        line["host_stream"] = {"tiles_bytes_per_layer": tiles_bytes,
-                               "achieved_GBps": tiles_bytes * a.layers / sec_per_step / 1e9}
+        achieved = tiles_bytes * a.layers / sec_per_step / 1e9
+        peak = host_copy_peak_gbps()
+        line["host_stream"] = {"tiles_bytes_per_layer": tiles_bytes, "achieved_GBps": achieved,
+                               "host_copy_peak_GBps": peak, "frac": achieved / peak,
+                               "peak_how": "one 2 GiB pinned host -> device copy, best of 3, CUDA events"}
     print(json.dumps(line), flush=True)
     for ly in layers:
         ly.close()

@@ -257,6 +257,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
+// Prefetch [p, p + bytes) into L2 (bulk, asynchronous, no completion to wait
+// for).  p 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Programmatic dependent launch.  Kernels of the forward path are launched
 // with launch_pdl; each calls pdl_wait() before it reads anything the
 // preceding kernel wrote (the wait returns once that grid has completed and
