@@ -11,8 +11,9 @@ Default workload: the DeepSeek-V3-shaped decode layer with T = 16 tokens
 tokens per second.
 
 Device timing: CUDA events around every step on the launching stream, after
-W warm-up steps; L2 is flushed (512 MiB write) between steps, outside the
-timed events.  The dominant kernel's duration comes from the library's
+W warm-up steps; L2 is flushed between steps, outside the timed events (a
+512 MiB write, then a 512 MiB read of another buffer, so that L2 holds
+clean lines unrelated to the layer).  The dominant kernel's duration comes from the library's
 stage events around that kernel alone, inside each timed step (an event
 between two kernels costs their programmatic-launch overlap, so the other
 stage boundaries carry none); the split over all stages is reported from
@@ -56,6 +57,25 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP8_OVER_BF16 = 2.0          # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 L2_FLUSH_BYTES = 512 << 20
+L2_NOTE = "flushed between steps (512 MiB written, then 512 MiB of another buffer read; outside the timed events)"
+
+
+class L2Flush:
+    """Evicts L2 between timed steps: writes a buffer four times the size of
+    L2, then reads another one of the same size.  After the write alone L2
+    is full of dirty lines, and the next step would pay for writing them
+    back to HBM as it allocates its own lines (about 130 MB, a third of a
+    one-token decode layer's own traffic); after the read the resident
+    lines are clean and belong to no input of the step."""
+
+    def __init__(self):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
 
 
 def parse():
@@ -263,7 +283,7 @@ def time_layer(a, layer, wl, x_np, steps, world, local):
     y = torch.empty_like(x)
     ws, nbytes = layer.workspace(T, mode)
     fwd = moe.moe_forward_decode if mode == moe.MODE_DECODE else moe.moe_forward_prefill
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    flush = L2Flush()
 
     def step():
         fwd(layer.handle, x.data_ptr(), T, y.data_ptr(), None, ws, nbytes, stream.cuda_stream)
@@ -278,7 +298,7 @@ def time_layer(a, layer, wl, x_np, steps, world, local):
         raise RuntimeError(f"device status {st} flags {flags:#x}")
 
     for _ in range(a.warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     use_graph = mode == moe.MODE_DECODE and not a.no_graph
@@ -288,7 +308,7 @@ def time_layer(a, layer, wl, x_np, steps, world, local):
     g_diag = moe.LayerStackGraph([layer.handle], mode, x, y) if use_graph else None
     diag = []
     for _ in range(max(3, a.warmup)):
-        flush.zero_()
+        flush()
         g_diag.replay() if g_diag is not None else step()
         diag.append(moe.moe_profile_read(layer.handle))
     torch.cuda.synchronize()
@@ -306,7 +326,7 @@ def time_layer(a, layer, wl, x_np, steps, world, local):
     if use_graph:
         graph = moe.LayerStackGraph([layer.handle], mode, x, y)
         for _ in range(a.warmup):
-            flush.zero_()
+            flush()
             graph.replay()
         torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
@@ -318,7 +338,7 @@ def time_layer(a, layer, wl, x_np, steps, world, local):
     with ClockSampler(local) as clk:
         t_wall = time.perf_counter()
         for i in range(steps):
-            flush.zero_()
+            flush()
             starts[i].record(stream)
             graph.replay() if graph is not None else step()
             ends[i].record(stream)
@@ -388,7 +408,7 @@ def time_layer(a, layer, wl, x_np, steps, world, local):
             moe.moe_forward_host(layer.handle, mode, xh.data_ptr(), T, yh.data_ptr(), ws_h, nb_h, stream.cuda_stream)
         e_ms = []
         for _ in range(steps):
-            flush.zero_()
+            flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             moe.moe_forward_host(layer.handle, mode, xh.data_ptr(), T, yh.data_ptr(), ws_h, nb_h, stream.cuda_stream)
@@ -421,7 +441,7 @@ def cpu_baseline_of(wl, inp_x, router_inp, target_s):
 def config_of(wl, world, graph):
     return {"workload": wl.name, "T": wl.T, "hidden": wl.hidden, "inter": wl.inter, "n_experts": wl.n_experts,
             "top_k": wl.top_k, "n_shared": wl.n_shared, "parallelism": f"replicas{world}", "graph": graph,
-            "l2": "flushed between steps (512 MiB write, outside the timed events)"}
+            "l2": L2_NOTE}
 
 
 # The prefill workload timed beside a decode workload of the same layer
@@ -551,9 +571,9 @@ def run_layers(a, wl):
         tiles_bytes = moe.moe_tiles_bytes(layers[0].handle)
     else:
         g = moe.LayerStackGraph([ly.handle for ly in layers], mode, x, y)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    flush = L2Flush()
     for _ in range(a.warmup):
-        flush.zero_()
+        flush()
         g.replay()
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
@@ -561,7 +581,7 @@ def run_layers(a, wl):
     cur = torch.cuda.current_stream()          # the graph replays on the current stream
     with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
         for i in range(a.steps):
-            flush.zero_()
+            flush()
             starts[i].record(cur)
             g.replay()
             ends[i].record(cur)
@@ -594,7 +614,7 @@ def run_layers(a, wl):
         "vs_baseline": None, "dtype": "fp8_e4m3", "data": "synthetic",
         "config": {"workload": wl.name, "T": T, "hidden": H, "inter": wl.inter, "n_experts": wl.n_experts,
                    "top_k": wl.top_k, "n_shared": wl.n_shared, "parallelism": "replicas1", "layers": a.layers,
-                   "graph": True, "l2": "flushed between steps (512 MiB write, outside the timed events)"},
+                   "graph": True, "l2": L2_NOTE},
         "roofline": roof, "cpu_baseline": None, "e2e": None, "gpu_launches": (6 if T <= 64 else 9) * a.layers * a.steps,
         "clocks": clk.summary(),
     }

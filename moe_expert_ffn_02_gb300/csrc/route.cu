@@ -17,12 +17,11 @@ namespace moe {
 // ---------------------------------------------------------------------------
 // Router logits for a decode batch (T <= 64): a GEMV over the fp32 router
 // weights, which dominate the bytes.  The channels are split into ksplit
-// slices (grid.y); a CTA stages its slice of x for up to GEMV_TC tokens in
-// shared memory and each of its 8 warps streams one expert's weight slice
-// with 16-byte loads, lane l taking channels 4l, 4l+128, ... in order.  The
-// lanes are combined by a fixed shuffle tree and the slice's partial sum
-// goes to part[slice][t][e]; the top-k kernel adds the slices in order, so
-// the result is deterministic.
+// slices (grid.y) and the experts into groups of 8 (grid.x); each CTA's
+// weight and x slices come into shared memory by bulk copies (no per-thread
+// load is in flight, so one round trip brings all of them), and the
+// slice's partial sum goes to part[slice][t][e]; the top-k kernel adds the
+// slices in order, so the result is deterministic.
 // ---------------------------------------------------------------------------
 constexpr int GEMV_WARPS = 8, GEMV_TC = 16;
 constexpr size_t PF_CHUNK = 64 << 10;   // bytes per L2 prefetch instruction
@@ -40,76 +39,148 @@ __device__ __forceinline__ void prefetch_shared_expert(const uint8_t* pf, size_t
     }
 }
 
-// One CTA's share of the split GEMV: warp w of the CTA takes expert e_base + w,
-// slice blockIdx.y of the channels.  Every thread of the CTA calls it (it
-// synchronises the CTA around the x staging).
-__device__ __forceinline__ void gemv_slice(const uint16_t* __restrict__ x, const float* __restrict__ W, int T, int H,
-                                           int E, int slice, int tc, float* __restrict__ part, uint16_t* xs,
-                                           int e_base) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = e_base + warp;
-    const int z = blockIdx.y;
-    const int h0 = z * slice;
-    const int n16 = slice / 8;                                   // 16-byte pieces per token row
-    for (int t0 = 0; t0 < T; t0 += tc) {
-        const int nt = min(tc, T - t0);
-        __syncthreads();
-        for (int i = threadIdx.x; i < nt * n16; i += blockDim.x) {
-            const int tt = i / n16, c = i - tt * n16;
-            *reinterpret_cast<uint4*>(xs + (size_t)tt * slice + c * 8) =
-                *reinterpret_cast<const uint4*>(x + (size_t)(t0 + tt) * H + h0 + c * 8);
-        }
-        __syncthreads();
-        if (e >= E) continue;
-        float acc[GEMV_TC];
-#pragma unroll
-        for (int u = 0; u < GEMV_TC; ++u) acc[u] = 0.f;
-        const float* wr = W + (size_t)e * H + h0;
-        // 8 weight loads of the lane in flight before the arithmetic that uses them
-        for (int c0 = lane * 4; c0 < slice; c0 += 8 * 128) {
-            float4 wv[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                wv[j] = (c0 + j * 128 < slice) ? __ldg(reinterpret_cast<const float4*>(wr + c0 + j * 128))
-                                               : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int c = c0 + j * 128;
-                if (c >= slice) break;
-#pragma unroll
-                for (int u = 0; u < GEMV_TC; ++u) {
-                    if (u < nt) {
-                        const uint2 raw = *reinterpret_cast<const uint2*>(xs + (size_t)u * slice + c);
-                        float p = __fmul_rn(__uint_as_float(raw.x << 16), wv[j].x);
-                        p = __fmaf_rn(__uint_as_float(raw.x & 0xFFFF0000u), wv[j].y, p);
-                        p = __fmaf_rn(__uint_as_float(raw.y << 16), wv[j].z, p);
-                        p = __fmaf_rn(__uint_as_float(raw.y & 0xFFFF0000u), wv[j].w, p);
-                        acc[u] = __fadd_rn(acc[u], p);
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < GEMV_TC; ++u) {
-            float v = acc[u];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
-            if (lane == 0 && u < nt) part[((size_t)z * T + t0 + u) * E + e] = v;
-        }
-    }
-}
+// One CTA's share of the split GEMV: experts e_base .. e_base + 7 (warp w
+// takes e_base + w), channels [z * slice, (z + 1) * slice) with z =
+// blockIdx.y.  Thread 0 moves every operand into shared memory with bulk
+// copies: the experts' weight rows in chunks of up to GEMV_WCH channels (two
+// buffers), the tokens' x slices per pass of up to tc tokens.  The first
+// weight chunk is issued before the programmatic-launch wait (the router
+// weights do not depend on the preceding kernel), and a single-chunk slice is
+// copied once for all passes.  Lane l accumulates channels 4l, 4l + 128, ...
+// of the slice in ascending order, one product chain of four channels at a
+// time; the lanes are combined by a fixed shuffle tree and the partial sum
+// goes to part[z][t][e].  A thread whose wait timed out skips its waits and
+// arithmetic from then on but still reaches every CTA barrier; nothing more is
+// written or issued, and the copies in flight land before the CTA exits.
+constexpr int GEMV_WCH = 1024;          // weight channels per chunk and expert (4 KB)
 
 __global__ void __launch_bounds__(GEMV_WARPS * 32) router_gemv_kernel(const uint16_t* __restrict__ x,
                                                                       const float* __restrict__ W, int T, int H,
                                                                       int E, int slice, int tc,
                                                                       float* __restrict__ part,
                                                                       const uint8_t* __restrict__ pf,
-                                                                      size_t pf_bytes) {
-    extern __shared__ __align__(16) uint16_t xs[];              // [tc][slice]
+                                                                      size_t pf_bytes, uint32_t* status,
+                                                                      uint32_t wait_limit) {
+    extern __shared__ __align__(128) uint8_t gsm[];
+    const int wch = min(slice, GEMV_WCH);                        // channels per chunk
+    const int nch = (slice + GEMV_WCH - 1) / GEMV_WCH;           // chunks per slice
+    float* wbuf = reinterpret_cast<float*>(gsm);                 // [nch > 1 ? 2 : 1][GEMV_WARPS][wch]
+    uint16_t* xs = reinterpret_cast<uint16_t*>(gsm + (size_t)(nch > 1 ? 2 : 1) * GEMV_WARPS * wch * 4);  // [tc][slice]
+    __shared__ uint64_t wbar[2], xbar;
+    __shared__ int abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int z = blockIdx.y, h0 = z * slice;
+    const int e_base = blockIdx.x * GEMV_WARPS;
+    const int ne = min(GEMV_WARPS, E - e_base);
+    const int e = e_base + warp;
     pdl_trigger();
+    if (threadIdx.x == 0) {
+        mbar_init(&wbar[0], 1);
+        mbar_init(&wbar[1], 1);
+        mbar_init(&xbar, 1);
+        fence_mbar_init();
+        abort_flag = 0;
+    }
+    __syncthreads();
+    volatile int* abort = &abort_flag;
+    // chunk c of the slice into buffer (c & 1): ne weight rows of cw channels
+    auto issue_w = [&](int c) {
+        const int cw = min(wch, slice - c * GEMV_WCH);
+        float* dst = wbuf + (size_t)(c & 1) * GEMV_WARPS * wch;
+        mbar_arrive_expect_tx(&wbar[c & 1], (uint32_t)(ne * cw * 4));
+        for (int w = 0; w < ne; ++w)
+            bulk_g2s(dst + (size_t)w * wch, W + (size_t)(e_base + w) * H + h0 + (size_t)c * GEMV_WCH, cw * 4,
+                     &wbar[c & 1]);
+    };
+    uint32_t wphase[2] = {0u, 0u}, xphase = 0u;
+    uint32_t pend = 0;                 // bit b: wbar[b] armed and not yet waited; bit 2: xbar
+    if (threadIdx.x == 0) {
+        issue_w(0);
+        pend |= 1u;
+    }
     prefetch_shared_expert(pf, pf_bytes);
     pdl_wait();
-    gemv_slice(x, W, T, H, E, slice, tc, part, xs, blockIdx.x * GEMV_WARPS);
+    bool dead = false;
+    for (int t0 = 0; t0 < T; t0 += tc) {
+        const int nt = min(tc, T - t0);
+        if (threadIdx.x == 0 && !dead) {
+            mbar_arrive_expect_tx(&xbar, (uint32_t)(nt * slice * 2));
+            for (int tt = 0; tt < nt; ++tt)
+                bulk_g2s(xs + (size_t)tt * slice, x + (size_t)(t0 + tt) * H + h0, slice * 2, &xbar);
+            pend |= 4u;
+        }
+        if (!dead) {
+            if (mbar_wait_bounded(&xbar, xphase, wait_limit, status, abort)) {
+                xphase ^= 1u;
+                if (threadIdx.x == 0) pend &= ~4u;
+            } else {
+                dead = true;
+            }
+        }
+        dead = __any_sync(0xFFFFFFFFu, dead);                      // warp-uniform (the shuffles below)
+        float acc[GEMV_TC];
+#pragma unroll
+        for (int u = 0; u < GEMV_TC; ++u) acc[u] = 0.f;
+        for (int c = 0; c < nch; ++c) {
+            const int b = c & 1;
+            if (nch > 1 && threadIdx.x == 0 && c + 1 < nch && !dead) {   // the next chunk into the other buffer
+                issue_w(c + 1);
+                pend |= 1u << ((c + 1) & 1);
+            }
+            // a single-chunk slice stays resident: its barrier is waited on in the first pass only
+            if ((nch > 1 || t0 == 0) && !dead) {
+                if (mbar_wait_bounded(&wbar[b], wphase[b], wait_limit, status, abort)) {
+                    wphase[b] ^= 1u;
+                    if (threadIdx.x == 0) pend &= ~(1u << b);
+                } else {
+                    dead = true;
+                }
+            }
+            dead = __any_sync(0xFFFFFFFFu, dead);
+            if (warp < ne && !dead) {
+                const float* wr = wbuf + ((size_t)b * GEMV_WARPS + warp) * wch;
+                const int cw = min(wch, slice - c * GEMV_WCH);
+                const int cbase = c * GEMV_WCH;
+                for (int cc = lane * 4; cc < cw; cc += 128) {
+                    const float4 wv = *reinterpret_cast<const float4*>(wr + cc);
+#pragma unroll
+                    for (int u = 0; u < GEMV_TC; ++u) {
+                        if (u < nt) {
+                            const uint2 raw = *reinterpret_cast<const uint2*>(xs + (size_t)u * slice + cbase + cc);
+                            float p = __fmul_rn(__uint_as_float(raw.x << 16), wv.x);
+                            p = __fmaf_rn(__uint_as_float(raw.x & 0xFFFF0000u), wv.y, p);
+                            p = __fmaf_rn(__uint_as_float(raw.y << 16), wv.z, p);
+                            p = __fmaf_rn(__uint_as_float(raw.y & 0xFFFF0000u), wv.w, p);
+                            acc[u] = __fadd_rn(acc[u], p);
+                        }
+                    }
+                }
+            }
+            if (nch > 1) __syncthreads();                          // buffer b free for chunk c + 2
+        }
+        if (warp < ne && !dead) {
+#pragma unroll
+            for (int u = 0; u < GEMV_TC; ++u) {
+                if (u < nt) {
+                    float v = acc[u];
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
+                    if (lane == 0) part[((size_t)z * T + t0 + u) * E + e] = v;
+                }
+            }
+        }
+        __syncthreads();                                           // xs (and a resident chunk) reused next pass
+        if (nch > 1 && t0 + tc < T && threadIdx.x == 0 && !dead) {   // the next pass starts from chunk 0 again
+            issue_w(0);
+            pend |= 1u;
+        }
+    }
+    // copies still in flight after a timeout land before the CTA exits
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < 2; ++b)
+            if ((pend >> b) & 1u) mbar_wait_bounded(&wbar[b], wphase[b], wait_limit, status, nullptr);
+        if (pend & 4u) mbar_wait_bounded(&xbar, xphase, wait_limit, status, nullptr);
+    }
 }
 
 // The shared expert's gate/up tile images (group E) to prefetch during the
@@ -143,10 +214,11 @@ cudaError_t launch_router_logits(const moe_layer* L, const uint16_t* x, int T, f
     const int H = L->d.hidden, E = L->d.n_experts;
     if (gemv) {                                        // decode batch: split GEMV, ksplit partial sums
         const int slice = H / ksplit;
-        const int tc = max(1, min(GEMV_TC, (160 * 1024) / (slice * 2)));
-        const size_t smem = (size_t)tc * slice * 2;
+        const int tc = max(1, min(GEMV_TC, (128 * 1024) / (slice * 2)));
+        const int nbuf = slice > GEMV_WCH ? 2 : 1;
+        const size_t smem = (size_t)nbuf * GEMV_WARPS * min(slice, GEMV_WCH) * 4 + (size_t)tc * slice * 2;
         {
-            cudaError_t e = ensure_smem_limit<router_gemv_kernel>(160 * 1024 + 4096);
+            cudaError_t e = ensure_smem_limit<router_gemv_kernel>(2 * GEMV_WARPS * GEMV_WCH * 4 + 128 * 1024);
             if (e != cudaSuccess) return e;
         }
         dim3 grid((E + GEMV_WARPS - 1) / GEMV_WARPS, ksplit);
@@ -154,7 +226,7 @@ cudaError_t launch_router_logits(const moe_layer* L, const uint16_t* x, int T, f
         size_t pf_bytes = 0;
         shared_expert_prefetch(L, T, &pf, &pf_bytes);
         return launch_pdl(router_gemv_kernel, grid, dim3(GEMV_WARPS * 32), smem, s, x, L->router_w, T, H, E, slice, tc,
-                          part, pf, pf_bytes);
+                          part, pf, pf_bytes, L->dev_status, L->wait_limit);
     }
     return launch_router_tc(L, x, T, part, ksplit, s);      // prefill batch: tensor-core GEMM (router_tc.cu)
 }
@@ -194,11 +266,20 @@ __device__ __forceinline__ float gate_exp(float x) {
 
 // ---------------------------------------------------------------------------
 // Top-k + gate weights, one warp per token.  Lane l holds experts
-// l, l+32, ...; each of the k rounds takes the warp-wide maximum of the
-// remaining logits, larger value first and lower index on ties (-0 == +0).
+// l, l+32, ...; each of the k rounds takes the largest remaining logit,
+// lower index on ties (-0 == +0; a NaN ranks below every number).  A round
+// is two warp reductions: the maximum of an order-preserving integer key of
+// the logits, then the minimum index among the lanes that hold it.
 // Weights: m = L[id0]; e_j = exp(L[id_j] - m); S = e_0 + e_1 + ... summed
-// left to right; w_j = e_j / S -- each step an IEEE-rounded fp32 op.
+// left to right; w_j = e_j / S -- each step an IEEE-rounded fp32 op (lane j
+// computes e_j and w_j; every lane forms S in the same order).
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t order_key(float v) {
+    if (v != v) return 1u;                                    // NaN: below every number
+    const uint32_t b = __float_as_uint(v == 0.0f ? 0.0f : v); // -0 -> +0
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);        // >= 0x007FFFFF for numbers
+}
+
 template <int PER>
 __device__ void topk_token(const float* __restrict__ part, int ksplit, const float* __restrict__ bias, int T, int E,
                            int k, float* __restrict__ logits_out, int32_t* __restrict__ ids,
@@ -225,51 +306,42 @@ __device__ void topk_token(const float* __restrict__ part, int ksplit, const flo
             for (int zz = 0; zz < ZB; ++zz)
                 if (z0 + zz < ksplit) v[i] = (z0 + zz == 0) ? pv[i][zz] : __fadd_rn(v[i], pv[i][zz]);
     }
+    uint32_t key[PER];                    // 0: not an expert, or already taken
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
         const int e = lane + 32 * i;
+        key[i] = 0u;
         if (e < E) {
             if (bias) v[i] = __fadd_rn(v[i], bias[e]);
             if (logits_out) logits_out[(size_t)t * E + e] = v[i];
-        } else {
-            v[i] = -CUDART_INF_F;
+            key[i] = order_key(v[i]);
         }
     }
-    uint32_t taken = 0;
     for (int j = 0; j < k; ++j) {
-        float bv = -CUDART_INF_F;
-        int bi = 0x7FFFFFFF;
+        uint32_t bk = 0u, bi = 0xFFFFFFFFu;
 #pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E && !((taken >> i) & 1u)) {
-                if (bi == 0x7FFFFFFF || v[i] > bv) { bv = v[i]; bi = e; }
-            }
-        }
+        for (int i = 0; i < PER; ++i)                      // the lane's best: lowest i among equal keys
+            if (key[i] > bk) { bk = key[i]; bi = (uint32_t)(lane + 32 * i); }
+        const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, bk);
+        const int win = (int)__reduce_min_sync(0xFFFFFFFFu, bk == m ? bi : 0xFFFFFFFFu);
+        if ((win & 31) == lane) {
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
-            const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
-            const bool better = (oi != 0x7FFFFFFF) &&
-                                (bi == 0x7FFFFFFF || ov > bv || (ov == bv && oi < bi));
-            if (better) { bv = ov; bi = oi; }
+            for (int i = 0; i < PER; ++i)
+                if (i == (win >> 5)) { key[i] = 0u; sel_v[j] = v[i]; }
+            sel_i[j] = win;
         }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        if (lane == 0) { sel_v[j] = bv; sel_i[j] = bi; }
     }
     __syncwarp();
-    if (lane == 0) {
-        const float m = sel_v[0];
-        float ev[MAX_TOPK];
-        float S = 0.0f;
-        for (int j = 0; j < k; ++j) {
-            ev[j] = gate_exp(__fsub_rn(sel_v[j], m));
-            S = (j == 0) ? ev[0] : __fadd_rn(S, ev[j]);
-        }
-        for (int j = 0; j < k; ++j) {
-            if (ids) ids[(size_t)t * k + j] = sel_i[j];
-            if (wout) wout[(size_t)t * k + j] = __fdiv_rn(ev[j], S);
-        }
+    const float m = sel_v[0];
+    const float ej = lane < k ? gate_exp(__fsub_rn(sel_v[lane], m)) : 0.f;
+    float S = 0.f;
+    for (int j = 0; j < k; ++j) {
+        const float ev = __shfl_sync(0xFFFFFFFFu, ej, j);
+        S = (j == 0) ? ev : __fadd_rn(S, ev);
+    }
+    if (lane < k) {
+        if (ids) ids[(size_t)t * k + lane] = sel_i[lane];
+        if (wout) wout[(size_t)t * k + lane] = __fdiv_rn(ej, S);
     }
     __syncwarp();
 }
@@ -387,21 +459,15 @@ __device__ int block_excl_scan_1024(int v, int* total) {
     return r;
 }
 
-// Offsets, padded offsets and the group table from the chunk counts; thread e
-// of the block handles expert e (blockDim.x >= E).
-__device__ void scan_groups(const int32_t* __restrict__ chunk_cnt, int n_chunks, int T, int E, int k, int n_shared,
-                            int bn, int32_t* __restrict__ chunk_base, int32_t* __restrict__ offsets,
-                            int32_t* __restrict__ offsets_pad, int32_t* __restrict__ offsets_out, GroupTable* gt) {
+// Offsets, padded offsets and the group table from the per-expert pair
+// counts; thread e of the block handles expert e (blockDim.x >= E) and
+// passes tot = expert e's count (0 for e >= E).  Returns expert e's first
+// row (*off_e) and first internal row (*poff_e).
+__device__ void scan_counts(int tot, int T, int E, int n_shared, int bn, int32_t* __restrict__ offsets,
+                            int32_t* __restrict__ offsets_pad, int32_t* __restrict__ offsets_out, GroupTable* gt,
+                            int* off_e, int* poff_e) {
     __shared__ int total_s;
     const int e = threadIdx.x;
-    int tot = 0;
-    if (e < E) {
-        for (int c = 0; c < n_chunks; ++c) {
-            const int v = chunk_cnt[(size_t)c * E + e];
-            chunk_base[(size_t)c * E + e] = tot;
-            tot += v;
-        }
-    }
     const int off = block_excl_scan_1024(e < E ? tot : 0, &total_s);
     const int R = total_s;
     // internal row space: every group starts on a multiple of ROW_ALIGN rows
@@ -412,13 +478,14 @@ __device__ void scan_groups(const int32_t* __restrict__ chunk_cnt, int n_chunks,
         offsets[e] = off;
         offsets_pad[e] = poff;
         if (offsets_out) offsets_out[e] = off;
-        for (int c = 0; c < n_chunks; ++c) chunk_base[(size_t)c * E + e] += off;
     }
     if (e == 0) {
         offsets[E] = R;
         offsets_pad[E] = shared_row0;
         if (offsets_out) offsets_out[E] = R;
     }
+    *off_e = off;
+    *poff_e = poff;
     // group table: the active routed experts in index order and the shared expert.  From
     // PF_MIN_TOKENS tokens on the shared expert comes first: its weights do not depend on the
     // routing, so the expert GEMMs start on them while the L2 prefetch of them issued during
@@ -459,6 +526,26 @@ __device__ void scan_groups(const int32_t* __restrict__ chunk_cnt, int n_chunks,
         gt->bn = bn;
         gt->total_rows = shared_row0 + (n_shared ? T : 0);
     }
+}
+
+// The same from the chunk counts of the multi-CTA grouping; also turns the
+// counts into every chunk's first row per expert (chunk_base).
+__device__ void scan_groups(const int32_t* __restrict__ chunk_cnt, int n_chunks, int T, int E, int k, int n_shared,
+                            int bn, int32_t* __restrict__ chunk_base, int32_t* __restrict__ offsets,
+                            int32_t* __restrict__ offsets_pad, int32_t* __restrict__ offsets_out, GroupTable* gt) {
+    const int e = threadIdx.x;
+    int tot = 0;
+    if (e < E) {
+        for (int c = 0; c < n_chunks; ++c) {
+            const int v = chunk_cnt[(size_t)c * E + e];
+            chunk_base[(size_t)c * E + e] = tot;
+            tot += v;
+        }
+    }
+    int off, poff;
+    scan_counts(tot, T, E, n_shared, bn, offsets, offsets_pad, offsets_out, gt, &off, &poff);
+    if (e < E)
+        for (int c = 0; c < n_chunks; ++c) chunk_base[(size_t)c * E + e] += off;
 }
 
 __global__ void __launch_bounds__(1024) perm_scan_kernel(const int32_t* __restrict__ chunk_cnt, int n_chunks, int T,
@@ -524,36 +611,73 @@ __global__ void __launch_bounds__(128) perm_scatter_kernel(const int32_t* __rest
 
 // ---------------------------------------------------------------------------
 // Routing of a decode batch (T <= CHUNK_TOK, E <= 512) in one CTA: top-k and
-// gate weights, then the grouping (count, scan, scatter) of the single
-// chunk -- the same device functions as the multi-CTA kernels above, so the
-// results are identical, with three kernel boundaries fewer.
+// gate weights (the device function of the multi-CTA top-k kernel), then the
+// grouping with the ids, counts and offsets held in shared memory.  Rows
+// inside an expert ascend with the pair index (token-major), as in the
+// multi-CTA grouping, so the results are identical to it.
 // ---------------------------------------------------------------------------
 constexpr int SMALL_THREADS = 512;
+constexpr int SMALL_PAIRS = CHUNK_TOK * MAX_TOPK;
 
 template <int PER>
 __global__ void __launch_bounds__(SMALL_THREADS) route_small_kernel(
     const float* __restrict__ part, int ksplit, const float* __restrict__ bias, int T, int E, int k, int n_shared,
     int bn, float* __restrict__ logits_out, int32_t* __restrict__ ids, float* __restrict__ wout,
-    int32_t* __restrict__ chunk_cnt, int32_t* __restrict__ chunk_base, int32_t* __restrict__ offsets,
-    int32_t* __restrict__ offsets_pad, int32_t* __restrict__ offsets_out, GroupTable* gt,
-    int32_t* __restrict__ sorted_token, int32_t* __restrict__ inv_row, int32_t* __restrict__ inv_int,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ offsets_pad, int32_t* __restrict__ offsets_out,
+    GroupTable* gt, int32_t* __restrict__ sorted_token, int32_t* __restrict__ inv_row, int32_t* __restrict__ inv_int,
     uint32_t* status) {
     __shared__ float sel_v[SMALL_THREADS / 32][MAX_TOPK];
     __shared__ int sel_i[SMALL_THREADS / 32][MAX_TOPK];
-    __shared__ int32_t cnt[512];
+    __shared__ int32_t s_ids[SMALL_PAIRS];
+    __shared__ int32_t cnt[512], s_off[512], s_pad[512];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_trigger();
+    for (int e = threadIdx.x; e < E; e += SMALL_THREADS) cnt[e] = 0;
     pdl_wait();
-    for (int t = warp; t < T; t += SMALL_THREADS / 32)
+    for (int t = warp; t < T; t += SMALL_THREADS / 32) {
         topk_token<PER>(part, ksplit, bias, T, E, k, logits_out, ids, wout, t, lane, sel_v[warp], sel_i[warp]);
+        if (lane < k) s_ids[t * k + lane] = sel_i[warp][lane];
+    }
     __syncthreads();
-    if (warp == 0) count_chunk(ids, T, E, k, 0, cnt, chunk_cnt, status, lane);
+    const int n = T * k;
+    for (int i = threadIdx.x; i < n; i += SMALL_THREADS) {
+        const int e = clamp_expert(s_ids[i], E, status);
+        s_ids[i] = e;
+        atomicAdd(&cnt[e], 1);
+    }
     __syncthreads();
-    scan_groups(chunk_cnt, 1, T, E, k, n_shared, bn, chunk_base, offsets, offsets_pad, offsets_out, gt);
+    {
+        const int e = threadIdx.x;
+        int off, poff;
+        scan_counts(e < E ? cnt[e] : 0, T, E, n_shared, bn, offsets, offsets_pad, offsets_out, gt, &off, &poff);
+        if (e < E) {
+            s_off[e] = off;
+            s_pad[e] = poff;
+            cnt[e] = 0;                        // reused as the running count per expert
+        }
+    }
     __syncthreads();
-    if (warp == 0)
-        scatter_chunk(ids, T, E, k, 0, chunk_base, offsets, offsets_pad, sorted_token, inv_row, inv_int, status, cnt,
-                      lane);
+    if (warp == 0) {
+        // stable ranks: 32 pairs at a time in pair order, equal experts ranked by a warp match
+        const uint32_t lt_mask = (1u << lane) - 1u;
+        for (int b0 = 0; b0 < n; b0 += 32) {
+            const int i = b0 + lane;
+            const bool valid = i < n;
+            const int e = valid ? s_ids[i] : -1 - lane;
+            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, e);
+            const int rank = __popc(peers & lt_mask);
+            if (valid) {
+                const int r = cnt[e] + rank;
+                const int row = s_off[e] + r;
+                if (sorted_token) sorted_token[row] = i / k;
+                inv_row[i] = row;
+                inv_int[i] = s_pad[e] + r;
+            }
+            __syncwarp();
+            if (valid && (peers & lt_mask) == 0) cnt[e] += __popc(peers);
+            __syncwarp();
+        }
+    }
 }
 
 cudaError_t launch_route_small(const moe_layer* L, const float* part, int ksplit, bool add_bias, int T,
@@ -566,7 +690,6 @@ cudaError_t launch_route_small(const moe_layer* L, const float* part, int ksplit
     if (per <= P) {                                                                                               \
         err = launch_pdl(route_small_kernel<P>, dim3(1), dim3(SMALL_THREADS), 0, s,                               \
             part, ksplit, add_bias ? L->router_b : nullptr, T, E, k, L->d.n_shared, bn, logits_out, ids, w,       \
-            reinterpret_cast<int32_t*>(ws + lay.chunk_cnt), reinterpret_cast<int32_t*>(ws + lay.chunk_base),      \
             reinterpret_cast<int32_t*>(ws + lay.offsets), reinterpret_cast<int32_t*>(ws + lay.offsets_pad),       \
             offsets_out, reinterpret_cast<GroupTable*>(ws + lay.table), sorted_out, inv_row,                      \
             reinterpret_cast<int32_t*>(ws + lay.inv_int), L->dev_status);                                         \
