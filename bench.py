@@ -371,7 +371,7 @@ def time_layer(a, layer, wl, x_np, steps, world, local):
         else:
             alg = n_touched * (H * wl.inter + (H // 128) * (wl.inter // 128) * 4) + rows * (wl.inter + 4 * H)
         achieved = alg / dom_s / 1e9
-        roof = {"bound": "hbm", "kernel": f"moe::expert_gemm_kernel<{1 if dom == 'gate_up' else 0}> ({dom})",
+        roof = {"bound": "hbm", "kernel": f"moe::dec::expert_dec_kernel<{1 if dom == 'gate_up' else 0}> ({dom})",
                 "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s", "frac": achieved / pk["hbm"],
                 "algorithmic_bytes_per_launch": alg, "peak_source": pk["src"],
                 "traffic": traffic_for(dom, wl.name)}

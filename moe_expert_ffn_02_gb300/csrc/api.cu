@@ -213,7 +213,8 @@ moe_status run_forward(moe_layer* L, int mode, const uint16_t* x, int T, uint16_
         return cap == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(L->ev[i], s, cudaEventRecordExternal)
                                                     : cudaEventRecord(L->ev[i], s);
     };
-    // prefill: tcgen05 grouped GEMMs (128-token tiles); decode: weight-streaming kernels (64-token tiles)
+    // prefill: tcgen05 grouped GEMMs (128-token tiles); decode: tcgen05 weight-streaming GEMMs with the
+    // weights as the 128-row operand (64-token tiles)
     const bool tc_path = (mode == MOE_MODE_PREFILL);
     MOE_CUDA(mark(0), "profile event");
     st = run_route(L, x, nullptr, T, lay, ws, dbg, s, tc_path ? moe::tc_tile_n() : kBN);
@@ -227,12 +228,12 @@ moe_status run_forward(moe_layer* L, int mode, const uint16_t* x, int T, uint16_
     MOE_CUDA(moe::launch_quant_scatter(L, x, T, lay, ws, dbg ? dbg->xq : nullptr, dbg ? dbg->sx : nullptr, s),
              "activation quantisation");
     MOE_CUDA(mark(2), "profile event");
-    MOE_CUDA(tc_path ? moe::launch_expert_tc_gate_up(L, T, lay, ws, s) : moe::launch_expert_gate_up(L, T, lay, ws, kBN, s),
+    MOE_CUDA(tc_path ? moe::launch_expert_tc_gate_up(L, T, lay, ws, s) : moe::launch_expert_dec_gate_up(L, T, lay, ws, kBN, s),
              "gate/up GEMM");
     if (dbg && (dbg->hq || dbg->sh))
         MOE_CUDA(moe::launch_h_gather(L, T, lay, ws, dbg->hq, dbg->sh, s), "h debug copy");
     MOE_CUDA(mark(3), "profile event");
-    MOE_CUDA(tc_path ? moe::launch_expert_tc_down(L, T, lay, ws, s) : moe::launch_expert_down(L, T, lay, ws, kBN, s),
+    MOE_CUDA(tc_path ? moe::launch_expert_tc_down(L, T, lay, ws, s) : moe::launch_expert_dec_down(L, T, lay, ws, kBN, s),
              "down GEMM");
     MOE_CUDA(mark(4), "profile event");
     if (cs.n_ranks == 1 && !cs.defer)

@@ -18,7 +18,7 @@ constexpr int MAX_TOPK = 32;
 constexpr int MAX_EXPERTS = 1024;
 constexpr int ROW_PAD = 256;          // spare rows after every permuted buffer
 constexpr int ROW_ALIGN = 8;          // each group's rows start on a multiple of 8
-constexpr int DEC_TILE_N = 64;        // token rows per group tile of the weight-streaming (decode) GEMMs;
+constexpr int DEC_TILE_N = 16;        // token rows per group tile of the weight-streaming (decode) GEMMs;
                                       // routing-only entries build their group table with it too
 
 // ---------------------------------------------------------------------------
@@ -286,16 +286,6 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
     return v;
 }
 
-// D = A(16x32 e4m3, row) * B(32x8 e4m3, col) + C, fp32 accumulate.
-__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                               uint32_t b0, uint32_t b1, const float (&c)[4]) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%10,%11,%12,%13};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
-}
-
 // Two fp32 -> two E4M3FN (round to nearest even, saturate to +-448);
 // `lo` lands in the low byte.
 __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
@@ -372,8 +362,9 @@ cudaError_t launch_permute(const moe_layer* L, const int32_t* ids, int T, const 
                            int32_t* offsets_out, int32_t* sorted_out, int32_t* inv_out, cudaStream_t s);
 cudaError_t launch_quant_scatter(const moe_layer* L, const uint16_t* x, int T, const WsLayout& lay, char* ws,
                                  uint8_t* xq_out, float* sx_out, cudaStream_t s);
-cudaError_t launch_expert_gate_up(const moe_layer* L, int T, const WsLayout& lay, char* ws, int bn, cudaStream_t s);
-cudaError_t launch_expert_down(const moe_layer* L, int T, const WsLayout& lay, char* ws, int bn, cudaStream_t s);
+cudaError_t launch_expert_dec_gate_up(const moe_layer* L, int T, const WsLayout& lay, char* ws, int bn,
+                                      cudaStream_t s);
+cudaError_t launch_expert_dec_down(const moe_layer* L, int T, const WsLayout& lay, char* ws, int bn, cudaStream_t s);
 cudaError_t launch_h_gather(const moe_layer* L, int T, const WsLayout& lay, char* ws, uint8_t* hq_out, float* sh_out,
                             cudaStream_t s);
 int tc_tile_n();
