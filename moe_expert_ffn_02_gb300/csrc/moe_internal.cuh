@@ -269,8 +269,11 @@ __device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
 // its memory is visible), so the launch, and whatever the kernel does before
 // the wait, overlaps the preceding kernel.  Small kernels call pdl_trigger()
 // on entry so their successor is launched at once; the persistent GEMMs
-// trigger by exiting.  Both are no-ops for a kernel launched without the
-// attribute.
+// trigger by exiting; the router kernels (the decode GEMV after its wait,
+// the prefill GEMM by exiting) release their successors only once the layer
+// input x is complete, so every later kernel of the layer may read x before
+// its own wait (the quantiser does).  Both are no-ops for a kernel launched
+// without the attribute.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

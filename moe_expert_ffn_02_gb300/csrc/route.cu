@@ -73,7 +73,6 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) router_gemv_kernel(const uint
     const int e_base = blockIdx.x * GEMV_WARPS;
     const int ne = min(GEMV_WARPS, E - e_base);
     const int e = e_base + warp;
-    pdl_trigger();
     if (threadIdx.x == 0) {
         mbar_init(&wbar[0], 1);
         mbar_init(&wbar[1], 1);
@@ -100,6 +99,9 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) router_gemv_kernel(const uint
     }
     prefetch_shared_expert(pf, pf_bytes);
     pdl_wait();
+    // the dependents launch only now, when the layer input x is complete: the quantiser reads x
+    // before its own wait
+    pdl_trigger();
     bool dead = false;
     for (int t0 = 0; t0 < T; t0 += tc) {
         const int nt = min(tc, T - t0);
@@ -280,8 +282,9 @@ __device__ __forceinline__ uint32_t order_key(float v) {
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);        // >= 0x007FFFFF for numbers
 }
 
+// `bias` may point to shared memory (a generic pointer: not read through the read-only path).
 template <int PER>
-__device__ void topk_token(const float* __restrict__ part, int ksplit, const float* __restrict__ bias, int T, int E,
+__device__ void topk_token(const float* __restrict__ part, int ksplit, const float* bias, int T, int E,
                            int k, float* __restrict__ logits_out, int32_t* __restrict__ ids,
                            float* __restrict__ wout, int t, int lane, float* sel_v, int* sel_i) {
     // logits: the ksplit partial sums added in split order, then the bias.  The
@@ -317,18 +320,37 @@ __device__ void topk_token(const float* __restrict__ part, int ksplit, const flo
             key[i] = order_key(v[i]);
         }
     }
-    for (int j = 0; j < k; ++j) {
-        uint32_t bk = 0u, bi = 0xFFFFFFFFu;
+    // each lane orders its PER candidates once (key descending, index ascending: insertion into
+    // a register list), then a round compares the lanes' heads and the winner pops its head
+    uint32_t hk[PER];
+    int hi[PER];
 #pragma unroll
-        for (int i = 0; i < PER; ++i)                      // the lane's best: lowest i among equal keys
-            if (key[i] > bk) { bk = key[i]; bi = (uint32_t)(lane + 32 * i); }
-        const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, bk);
-        const int win = (int)__reduce_min_sync(0xFFFFFFFFu, bk == m ? bi : 0xFFFFFFFFu);
-        if ((win & 31) == lane) {
+    for (int i = 0; i < PER; ++i) { hk[i] = 0u; hi[i] = 0x7FFFFFFF; }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        uint32_t ck = key[i];
+        int ci = lane + 32 * i;                            // indices of a lane ascend with i
+#pragma unroll
+        for (int p = 0; p <= i; ++p) {                     // equal keys: the lower index first
+            if (ck > hk[p] || (ck == hk[p] && ci < hi[p])) {
+                const uint32_t tk = hk[p]; const int ti = hi[p];
+                hk[p] = ck; hi[p] = ci;
+                ck = tk; ci = ti;
+            }
+        }
+    }
+    for (int j = 0; j < k; ++j) {
+        const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, hk[0]);
+        const int win = (int)__reduce_min_sync(0xFFFFFFFFu, hk[0] == m ? (uint32_t)hi[0] : 0xFFFFFFFFu);
+        if (win == hi[0]) {
 #pragma unroll
             for (int i = 0; i < PER; ++i)
-                if (i == (win >> 5)) { key[i] = 0u; sel_v[j] = v[i]; }
+                if (i == (win >> 5)) sel_v[j] = v[i];
             sel_i[j] = win;
+#pragma unroll
+            for (int p = 0; p + 1 < PER; ++p) { hk[p] = hk[p + 1]; hi[p] = hi[p + 1]; }
+            hk[PER - 1] = 0u;
+            hi[PER - 1] = 0x7FFFFFFF;
         }
     }
     __syncwarp();
@@ -630,12 +652,19 @@ __global__ void __launch_bounds__(SMALL_THREADS) route_small_kernel(
     __shared__ int sel_i[SMALL_THREADS / 32][MAX_TOPK];
     __shared__ int32_t s_ids[SMALL_PAIRS];
     __shared__ int32_t cnt[512], s_off[512], s_pad[512];
+    __shared__ float s_bias[512];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_trigger();
-    for (int e = threadIdx.x; e < E; e += SMALL_THREADS) cnt[e] = 0;
+    // the router bias is a layer constant: fetched before the wait, off the critical path
+    for (int e = threadIdx.x; e < E; e += SMALL_THREADS) {
+        cnt[e] = 0;
+        if (bias) s_bias[e] = bias[e];
+    }
+    __syncthreads();
     pdl_wait();
     for (int t = warp; t < T; t += SMALL_THREADS / 32) {
-        topk_token<PER>(part, ksplit, bias, T, E, k, logits_out, ids, wout, t, lane, sel_v[warp], sel_i[warp]);
+        topk_token<PER>(part, ksplit, bias ? s_bias : nullptr, T, E, k, logits_out, ids, wout, t, lane, sel_v[warp],
+                        sel_i[warp]);
         if (lane < k) s_ids[t * k + lane] = sel_i[warp][lane];
     }
     __syncthreads();
@@ -758,6 +787,32 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __re
     const int t = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_trigger();
+    // x is read and quantised before the wait: this kernel is launched only after the router
+    // kernel has passed its own wait, so the layer input is complete; only the destination rows
+    // come from the routing
+    const int G = H / QB;
+    uint32_t qv[QUANT_GPW];
+    float scv[QUANT_GPW];
+    {
+        uint2 raws[QUANT_GPW];
+#pragma unroll
+        for (int i = 0; i < QUANT_GPW; ++i) {
+            const int g = blockIdx.y * 8 * QUANT_GPW + warp + 8 * i;
+            raws[i] = g < G ? *reinterpret_cast<const uint2*>(x + (size_t)t * H + g * QB + lane * 4) : make_uint2(0u, 0u);
+        }
+#pragma unroll
+        for (int i = 0; i < QUANT_GPW; ++i) {
+            const uint2 raw = raws[i];
+            const float v0 = __uint_as_float(raw.x << 16), v1 = __uint_as_float(raw.x & 0xFFFF0000u);
+            const float v2 = __uint_as_float(raw.y << 16), v3 = __uint_as_float(raw.y & 0xFFFF0000u);
+            float am = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, off));
+            const float sc = (am > 0.f) ? __fdiv_rn(am, 448.0f) : 1.0f;
+            scv[i] = sc;
+            qv[i] = pack4_e4m3(__fdiv_rn(v0, sc), __fdiv_rn(v1, sc), __fdiv_rn(v2, sc), __fdiv_rn(v3, sc));
+        }
+    }
     pdl_wait();
     const int nd = k + (n_shared ? 1 : 0);
     if (threadIdx.x < k) {
@@ -769,26 +824,12 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __re
     }
     if (threadIdx.x == 0 && n_shared) dest[k] = offsets_pad[E] + t;
     __syncthreads();
-    const int G = H / QB;
-    // warp w of CTA (t, y) quantises groups 32y + w + 8i, i < QUANT_GPW; their loads are issued first
-    uint2 raws[QUANT_GPW];
-#pragma unroll
-    for (int i = 0; i < QUANT_GPW; ++i) {
-        const int g = blockIdx.y * 8 * QUANT_GPW + warp + 8 * i;
-        raws[i] = g < G ? *reinterpret_cast<const uint2*>(x + (size_t)t * H + g * QB + lane * 4) : make_uint2(0u, 0u);
-    }
 #pragma unroll
     for (int i = 0; i < QUANT_GPW; ++i) {
         const int g = blockIdx.y * 8 * QUANT_GPW + warp + 8 * i;
         if (g >= G) break;
-        const uint2 raw = raws[i];
-        const float v0 = __uint_as_float(raw.x << 16), v1 = __uint_as_float(raw.x & 0xFFFF0000u);
-        const float v2 = __uint_as_float(raw.y << 16), v3 = __uint_as_float(raw.y & 0xFFFF0000u);
-        float a = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
-        const float sc = (a > 0.f) ? __fdiv_rn(a, 448.0f) : 1.0f;
-        const uint32_t q = pack4_e4m3(__fdiv_rn(v0, sc), __fdiv_rn(v1, sc), __fdiv_rn(v2, sc), __fdiv_rn(v3, sc));
+        const uint32_t q = qv[i];
+        const float sc = scv[i];
         for (int d = 0; d < nd; ++d) {
             const int row = dest[d];
             if (row < 0) continue;
