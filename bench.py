@@ -177,24 +177,31 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.rows)}
 
 
-def kernel_source_hash() -> str:
+# the source file of each timed GEMM; its traffic record is tied to that file and the shared headers
+KERNEL_SOURCES = {"decode": "expert_dec.cu", "prefill": "expert_tc.cu"}
+SHARED_HEADERS = ("moe_internal.cuh", "tcgen05.cuh")
+
+
+def kernel_source_hash(path_kind: str) -> str:
+    """Hash of the sources one GEMM kernel is compiled from (its file and the
+    shared headers): a committed DRAM-traffic figure stays valid while they
+    are unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "moe_expert_ffn_02_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in (KERNEL_SOURCES[path_kind],) + SHARED_HEADERS:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def traffic_for(kernel: str, workload: str):
+def traffic_for(kernel: str, workload: str, path_kind: str):
     """dram bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel sources; else None."""
+    the current sources of that kernel; else None."""
     try:
         d = json.load(open(TRAFFIC_FILE))
     except Exception:
         return None
     e = d.get(workload, {}).get(kernel)
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or e.get("source_hash") != kernel_source_hash(path_kind):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -374,7 +381,7 @@ def time_layer(a, layer, wl, x_np, steps, world, local):
         roof = {"bound": "hbm", "kernel": f"moe::dec::expert_dec_kernel<{1 if dom == 'gate_up' else 0}> ({dom})",
                 "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s", "frac": achieved / pk["hbm"],
                 "algorithmic_bytes_per_launch": alg, "peak_source": pk["src"],
-                "traffic": traffic_for(dom, wl.name)}
+                "traffic": traffic_for(dom, wl.name, "decode")}
     else:
         flops_all = roofline.layer_flops(T, H, wl.inter, wl.top_k, wl.n_shared)
         alg = flops_all * (2 / 3 if dom == "gate_up" else 1 / 3)
@@ -384,7 +391,7 @@ def time_layer(a, layer, wl, x_np, steps, world, local):
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "algorithmic_flops_per_launch": alg,
                 "peak_source": f"{pk['src']} bf16 burst x {FP8_OVER_BF16} (nominal fp8/bf16 dense ratio)",
-                "traffic": traffic_for(dom, wl.name)}
+                "traffic": traffic_for(dom, wl.name, "prefill")}
 
     # ---------------------------------------------- the whole layer against the same peak (the targets are
     # stated per layer: touched-expert bytes / layer time for decode, expert FLOP / layer time for prefill)

@@ -128,12 +128,17 @@ def test_bench_metric_helpers():
     # oracle sample scaled to the workload's unit
     assert abs(bench.cpu_value(dec, 2.0, 4) - 2.0 / 4 * 16 * 1e6) < 1e-3
     assert abs(bench.cpu_value(pre, 2.0, 100) - 50.0) < 1e-12
-    # traffic: only when the committed capture was taken on the current kernel sources
-    h = bench.kernel_source_hash()
-    assert h == bench.kernel_source_hash() and len(h) == 16
+    # traffic: only when the committed capture was taken on the current sources of that kernel
+    hd, hp = bench.kernel_source_hash("decode"), bench.kernel_source_hash("prefill")
+    assert hd == bench.kernel_source_hash("decode") and len(hd) == 16 and hd != hp
     d = json.load(open(bench.TRAFFIC_FILE))
     for wl_name, per in d.items():
+        kind = "decode" if "decode" in wl_name else "prefill"
+        h = hd if kind == "decode" else hp
         for kernel, e in per.items():
-            got = bench.traffic_for(kernel, wl_name)
+            got = bench.traffic_for(kernel, wl_name, kind)
             assert got == (e["dram_bytes_per_launch"] if e["source_hash"] == h else None)
-    assert bench.traffic_for("gate_up", "no_such_workload") is None
+            # a record never applies to the other path's kernel
+            if e["source_hash"] == h:
+                assert bench.traffic_for(kernel, wl_name, "prefill" if kind == "decode" else "decode") is None
+    assert bench.traffic_for("gate_up", "no_such_workload", "decode") is None
