@@ -254,6 +254,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_dec_kernel(Args a) {
             for (int i = 0; i < TN; ++i) { acc0[i] = 0.f; acc1[i] = 0.f; }
             for (int kb = 0; kb < KT; ++kb) {
                 if (!dead && !mbar_wait_bounded(&tfull[buf], tphase, a.wait_limit, a.status, abort)) dead = true;
+                dead = __any_sync(0xFFFFFFFFu, dead);      // warp-uniform: tcgen05.ld is warp-collective
                 // the block's MMAs are done: its stage can be refilled
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[slot]);

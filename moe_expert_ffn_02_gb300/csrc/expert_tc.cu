@@ -241,6 +241,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) expert_tc_kernel(Args a) {
             for (int c = 0; c < HALF; ++c) acc[c] = 0.f;
             for (int kb = 0; kb < KT; ++kb) {
                 if (!dead && !mbar_wait_bounded(&tfull[buf], tphase, a.wait_limit, a.status, abort)) dead = true;
+                dead = __any_sync(0xFFFFFFFFu, dead);      // warp-uniform: tcgen05.ld is warp-collective
                 if (!dead) {
                     tc_fence_after();
                     // this block's scales from its stage's slot: s_x of my token, the record's weight
