@@ -222,8 +222,9 @@ moe_status moe_route_from_logits_noalloc(moe_layer* layer, const float* logits, 
 moe_status moe_forward_prefill(moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y,
                                const moe_route_out* dbg, void* ws, size_t ws_bytes, void* stream);
 
-/* The same function for 1 <= T <= MOE_DECODE_MAX_T tokens, on the
- * weight-streaming decode kernels.  Enqueues a fixed sequence of kernels
+/* The same function for 1 <= T <= MOE_DECODE_MAX_T tokens, on the decode
+ * kernels (one-CTA routing; expert GEMMs that stream only the touched
+ * experts' weights, with 16-token tiles).  Enqueues a fixed sequence of kernels
  * whose grids do not depend on the routing and reads nothing back to the
  * host, so a CUDA graph may capture it. */
 moe_status moe_forward_decode(moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y,

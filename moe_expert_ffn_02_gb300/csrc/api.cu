@@ -38,7 +38,7 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 inline size_t up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 constexpr uint32_t kDefaultWaitLimitUs = 2000000u;   // 2 s per bounded wait
-constexpr int kBN = moe::DEC_TILE_N;                 // n tile of the weight-streaming expert GEMMs
+constexpr int kBN = moe::DEC_TILE_N;                 // token tile of the decode expert GEMMs
 
 moe::WsLayout make_layout(const moe_layer* L, int T, int mode) {
     moe::WsLayout l{};
@@ -214,7 +214,7 @@ moe_status run_forward(moe_layer* L, int mode, const uint16_t* x, int T, uint16_
                                                     : cudaEventRecord(L->ev[i], s);
     };
     // prefill: tcgen05 grouped GEMMs (128-token tiles); decode: tcgen05 weight-streaming GEMMs with the
-    // weights as the 128-row operand (64-token tiles)
+    // weights as the 128-row operand (16-token tiles)
     const bool tc_path = (mode == MOE_MODE_PREFILL);
     MOE_CUDA(mark(0), "profile event");
     st = run_route(L, x, nullptr, T, lay, ws, dbg, s, tc_path ? moe::tc_tile_n() : kBN);

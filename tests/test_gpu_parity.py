@@ -140,8 +140,8 @@ def test_determinism_and_token_permutation(h):
     perm = np.random.default_rng(3).permutation(wl.T)
     yp, _ = h.run_forward(layer, inp["x"][perm], 1, want_dbg=False)
     assert np.array_equal(yp, y1[perm])
-    # decode (weight-streaming mma.sync kernels) and prefill (tcgen05 kernels)
-    # compute the same function with different summation orders
+    # decode (16-token tiles, weights as the 128-row MMA operand) and prefill
+    # (128-token tiles) compute the same function with different summation orders
     yd, _ = h.run_forward(layer, inp["x"][:64], 2, want_dbg=False)
     yq, _ = h.run_forward(layer, inp["x"][:64], 1, want_dbg=False)
     a, b = synth.bf16_to_f32(yd).astype(np.float64), synth.bf16_to_f32(yq).astype(np.float64)
